@@ -1,0 +1,30 @@
+"""Compile the CPU oracle (plain C, float64) into ``oracle/liboracle.so``.
+
+Test infrastructure: only the tests, the smoke check and the benchmark's CPU
+baseline load the result.
+"""
+from __future__ import annotations
+
+import os
+import subprocess
+import sys
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "yoco_oracle.c")
+LIB = os.path.join(HERE, "liboracle.so")
+
+
+def build(force: bool = False) -> str:
+    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= os.path.getmtime(SRC):
+        return LIB
+    tmp = LIB + f".tmp{os.getpid()}"
+    # No fast-math: the oracle keeps IEEE double semantics.
+    cmd = ["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-pthread", "-Wall", "-Wextra",
+           "-o", tmp, SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(force="--force" in sys.argv))
