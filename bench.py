@@ -1,0 +1,478 @@
+#!/usr/bin/env python3
+"""Benchmark of the YOCO cross-decoder hot path on GB300.
+
+One step = one scheduling step of the workload through the whole path:
+yoco_kv_append (the step's new shared K^/V^), yoco_select_cross_rows, then
+yoco_cross_attn_paged once per cross-decoder layer against the one shared
+cache. Inputs are seeded synthetic data resident in HBM before timing.
+
+Prints one JSON line (rank 0). Metric: KV GB/s read by the cross-decoder
+attention (logical bytes: every layer re-reads each row's causal K/V), its
+fraction of the measured HBM peak, and query rows/s.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1] [--impl ours|reference]
+
+Under torchrun each rank runs an independent replica (requests are
+independent; no collective is on the data path) and the slowest rank's time
+is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "cross-decoder paged attn: KV GB/s (% of HBM peak), query rows/s at 1 GB300"
+FALLBACK_HBM_GBS = 6800.0
+DOMINANT_KERNEL = "attn_split_tc"
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.txt")
+
+
+# ------------------------------------------------------------------ helpers
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", type=int, default=1, help="workload index 0..4 (1 = pure decode)")
+    ap.add_argument("--reqs", type=int, default=None, help="smaller case: override request count")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--seed-offset", type=int, default=0)
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def make_workload(config: int, rank: int = 0, reqs=None, seed_offset: int = 0):
+    """Replica `rank` of workload `config`: same shapes, its own seed."""
+    import workloads as W
+    base = {0: 1000, 1: 1001, 2: 1002, 3: 1003, 4: 1004}[config] + 7919 * (rank + seed_offset)
+    if config == 0:
+        return W.toy_r1r2(base)
+    if config == 1:
+        return W.pure_decode(base, **({} if reqs is None else {"num_reqs": reqs}))
+    if config == 2:
+        return W.mixed_step(base, **({} if reqs is None else {"n_decode": reqs}))
+    if config == 3:
+        return W.long_context(base, **({} if reqs is None else {"num_reqs": reqs}))
+    return W.shared_prefix(base, **({} if reqs is None else {"num_reqs": reqs}))
+
+
+def cross_rows_kv_lens(step) -> np.ndarray:
+    """Keys attended by each cross row (accounting only: bytes and rows for the metric)."""
+    qsl = np.asarray(step.query_start_loc, dtype=np.int64)
+    q_len = np.diff(qsl)
+    want = np.ones_like(q_len) if step.rows_per_req is None else np.asarray(step.rows_per_req)
+    k = np.minimum(np.maximum(want, 0), np.maximum(q_len, 0))
+    lens = []
+    for r, kr in enumerate(k):
+        for i in range(int(kr)):
+            lens.append(int(step.seq_lens[r]) - int(kr) + i + 1)
+    return np.asarray(lens, dtype=np.int64)
+
+
+def accounting(wl, step) -> dict:
+    """Algorithmic bytes of one step (per layer and per step)."""
+    from workloads import elem_bytes
+    sz = elem_bytes(wl.dtype)
+    kv = cross_rows_kv_lens(step)
+    rows = int(kv.shape[0])
+    kv_bytes_layer = int(kv.sum()) * 2 * wl.num_kv_heads * wl.head_dim * sz
+    qo_bytes_layer = 2 * rows * wl.num_q_heads * wl.head_dim * sz
+    bt_bytes_layer = 4 * int(np.sum((kv + wl.block_size - 1) // wl.block_size)) * wl.num_kv_heads
+    append_bytes = 2 * 2 * step.num_tokens * wl.num_kv_heads * wl.head_dim * sz  # read + write
+    return {
+        "rows": rows,
+        "kv_bytes_layer": kv_bytes_layer,
+        "attn_bytes_layer": kv_bytes_layer + qo_bytes_layer + bt_bytes_layer,
+        "kv_bytes_step": kv_bytes_layer * wl.layers,
+        "append_bytes_step": append_bytes,
+        "layers": wl.layers,
+    }
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    except (OSError, ValueError, KeyError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
+
+
+def kernel_source_sha() -> str:
+    src = os.path.join(ROOT, "yoco_shared_kv_gb300", "csrc", "cross_attn.cu")
+    with open(src, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, if it was taken on this workload with the current kernel source."""
+    try:
+        lines = open(PROFILE_TRAFFIC).read().splitlines()
+    except OSError:
+        return None
+    kv = dict(l.split("=", 1) for l in lines if "=" in l and not l.startswith("#"))
+    if kv.get("source_sha") != kernel_source_sha() or kv.get("workload") != workload:
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while work runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        self.t_start = self.t_stop = None
+
+    def mark_start(self):
+        self.t_start = time.time()
+
+    def mark_stop(self):
+        self.t_stop = time.time()
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for row in csv.reader(io.StringIO(out)):
+            if len(row) < 9:
+                continue
+            try:
+                sm.append(float(row[1]))
+                smax.append(float(row[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, row[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------- our arm
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    from yoco_shared_kv_gb300 import build as B
+    if rank == 0 or not os.path.exists(B.LIB):
+        B.build()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    from yoco_shared_kv_gb300 import _native as N
+    from yoco_shared_kv_gb300 import pipeline as P
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = make_workload(args.config, rank, args.reqs, args.seed_offset)
+    dw = P.DeviceWorkload(wl, dev, pin_host=not args.no_e2e, sentinel=False)
+    step_i = len(wl.steps) - 1
+    ds = dw.steps[step_i]
+    acc = accounting(wl, wl.steps[step_i])
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        dw.run_fill(stream)
+        for i in range(step_i):  # earlier steps of a multi-step schedule
+            dw.run_step(i, stream)
+    stream.synchronize()
+
+    ws_bytes = ds.workspace.numel() if ds.workspace is not None else 0
+    merges = 1 if N.yoco_cross_attn_workspace_size(max(ds.rows_upper, 1), wl.num_q_heads,
+                                                   wl.num_kv_heads, wl.head_dim, wl.block_size,
+                                                   ds.max_seq_len, P.torch_dtype(wl.dtype)) > 0 else 0
+    launches_per_step = 2 + wl.layers * (1 + merges)
+
+    sampler = None if args.no_clocks else ClockSampler(local)
+    # warm-up
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            dw.run_step(step_i, stream)
+    stream.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    L = wl.layers
+    # one event pair around every attention call of every timed step, read
+    # back after the timed region (no host synchronisation inside it)
+    attn_ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(L)] for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.mark_start()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for k in range(args.steps):
+            dw.append(ds, stream)
+            dw.select(ds, stream)
+            for layer in range(L):
+                attn_ev[k][layer][0].record(stream)
+                dw.attend(ds, layer, stream)
+                attn_ev[k][layer][1].record(stream)
+        ev1.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.mark_stop()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    attn_launch_ms = sum(a.elapsed_time(b) for row in attn_ev for a, b in row) / (args.steps * L)
+
+    max_ms = elapsed_ms
+    total_kv_bytes = acc["kv_bytes_step"] * args.steps
+    total_rows = acc["rows"] * L * args.steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([elapsed_ms, float(total_kv_bytes), float(total_rows)], dtype=torch.float64,
+                         device=dev)
+        tmax = t.clone()
+        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
+        dist.all_reduce(t, op=dist.ReduceOp.SUM)
+        max_ms = float(tmax[0])
+        total_kv_bytes, total_rows = float(t[1]), float(t[2])
+    clocks = sampler.stop() if sampler else None
+    if dw.error_bits() != 0:
+        raise RuntimeError(f"device error bits {dw.error_bits():#x}")
+
+    # end to end through the C ABI: pinned host inputs -> device, step, outputs -> host
+    e2e = None
+    if not args.no_e2e:
+        out_host = torch.empty(ds.out.shape, dtype=ds.out.dtype, pin_memory=True)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        k_e2e = max(1, min(args.steps, 200))
+        h2d = d2h = 0
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                ds.h2d(stream)
+                dw.run_step(step_i, stream)
+                out_host.copy_(ds.out, non_blocking=True)
+            stream.synchronize()
+            e0.record(stream)
+            for _ in range(k_e2e):
+                h2d = ds.h2d(stream)
+                dw.run_step(step_i, stream)
+                out_host.copy_(ds.out, non_blocking=True)
+                d2h = out_host.numel() * out_host.element_size()
+            e1.record(stream)
+        stream.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / k_e2e
+        if world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t[0])
+        e2e = {"value": round(total_kv_bytes / args.steps / (e2e_ms / 1e3) / 1e9, 3), "unit": "GB/s",
+               "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h)}
+
+    ms_per_step = max_ms / args.steps
+    value = total_kv_bytes / (max_ms / 1e3) / 1e9
+    peaks = measured_peaks()
+    achieved = acc["attn_bytes_layer"] / (attn_launch_ms / 1e3) / 1e9
+    traffic = profiled_traffic(wl.name)
+    res = {
+        "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "data": "synthetic (seeded N(0,1) K/V and queries, random page permutation)",
+        "config": {
+            "workload": wl.name, "description": wl.description, "H_q": wl.num_q_heads,
+            "H_kv": wl.num_kv_heads, "head_dim": wl.head_dim, "block_size": wl.block_size,
+            "layers": wl.layers, "requests": wl.steps[step_i].num_reqs,
+            "step_tokens": wl.steps[step_i].num_tokens, "cross_rows": acc["rows"],
+            "kv_bytes_per_layer": acc["kv_bytes_layer"],
+            "l2": ("inputs larger than L2" if acc["kv_bytes_layer"] > 129e6
+                   else "inputs fit in L2 (layers re-read them: logical bytes)"),
+            "parallelism": f"replicas x{world}",
+        },
+        "hbm_frac": round(value / peaks["hbm_gbs"], 4),
+        "query_rows_per_s": round(total_rows / (max_ms / 1e3), 1),
+        "roofline": {"kernel": DOMINANT_KERNEL + " (+ split merge)", "bound": "hbm",
+                     "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+                     "algorithmic_bytes_per_launch": acc["attn_bytes_layer"],
+                     "launch_ms": round(attn_launch_ms, 5), "peak_source": peaks["source"]},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if e2e is not None:
+        res["e2e"] = e2e
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(wl, step_i)
+    return res
+
+
+# ------------------------------------------------------------ oracle (CPU)
+
+
+def host_cores() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_step(wl, step, Ks, Vs, kp, vp, nthreads, layers=None, rows=None):
+    """One step through the CPU oracle: append, select, attention per layer."""
+    import oracle
+    oracle.kv_append(step.k_new, step.v_new, kp, vp, step.block_table, step.seq_lens,
+                     step.query_start_loc, wl.block_size)
+    _, cqsl, _ = oracle.select_cross_rows(step.query_start_loc, step.rows_per_req)
+    for layer in (range(wl.layers) if layers is None else layers):
+        q = oracle.widen(step.q[layer], wl.dtype)
+        oracle.cross_attn(q, Ks, Vs, step.seq_lens, cqsl, wl.scale, rows=rows, nthreads=nthreads)
+
+
+def _oracle_setup(wl, step, rows):
+    import oracle
+    reqs = sorted(set(step.req_ids[i] for i in range(step.num_reqs)))
+    del reqs
+    Ks, Vs = [], []
+    for r in step.req_ids:
+        K, V = wl.request_kv(r)
+        Ks.append(oracle.widen(K, wl.dtype))
+        Vs.append(oracle.widen(V, wl.dtype))
+    return Ks, Vs
+
+
+def cpu_baseline(wl, step_i: int, budget_s: float = 20.0) -> dict:
+    """The oracle timed on this host's cores over a bounded sample of the step."""
+    step = wl.steps[step_i]
+    acc = accounting(wl, step)
+    nthreads = host_cores()
+    Ks, Vs = _oracle_setup(wl, step, None)
+    kp, vp = wl.empty_pool(), wl.empty_pool()
+    kv_lens = cross_rows_kv_lens(step)
+    # sample: all rows, layers taken one at a time until the budget is spent
+    t0 = time.perf_counter()
+    done = 0
+    for layer in range(wl.layers):
+        oracle_step(wl, step, Ks, Vs, kp, vp, nthreads, layers=[layer])
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    kv_bytes = acc["kv_bytes_layer"] * done
+    return {"value": round(kv_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": nthreads,
+            "kind": "oracle",
+            "sample": f"{acc['rows']} rows x {done} of {wl.layers} layers of {wl.name} "
+                      f"(sum kv_len {int(kv_lens.sum())}), float64, {dt:.1f} s",
+            "query_rows_per_s": round(acc["rows"] * done / dt, 3)}
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: same metric/config, host cores, bounded steps."""
+    wl = make_workload(args.config, 0, args.reqs, args.seed_offset)
+    step_i = len(wl.steps) - 1
+    step = wl.steps[step_i]
+    acc = accounting(wl, step)
+    nthreads = host_cores()
+    Ks, Vs = _oracle_setup(wl, step, None)
+    kp, vp = wl.empty_pool(), wl.empty_pool()
+    # a reference step is the step's append + select + a bounded number of
+    # layers over all rows, sized so the whole run stays within minutes
+    t0 = time.perf_counter()
+    oracle_step(wl, step, Ks, Vs, kp, vp, nthreads, layers=[0])
+    one = time.perf_counter() - t0
+    budget_per_step = 120.0 / max(1, args.steps + args.warmup)
+    layers = max(1, min(wl.layers, int(budget_per_step / max(one, 1e-6))))
+    for _ in range(args.warmup):
+        oracle_step(wl, step, Ks, Vs, kp, vp, nthreads, layers=range(layers))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(wl, step, Ks, Vs, kp, vp, nthreads, layers=range(layers))
+    dt = time.perf_counter() - t0
+    kv_bytes = acc["kv_bytes_layer"] * layers * args.steps
+    value = kv_bytes / dt / 1e9
+    sample = f"{acc['rows']} rows x {layers} of {wl.layers} layers per step of {wl.name}"
+    return {
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": wl.name, "description": wl.description},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": nthreads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "query_rows_per_s": round(acc["rows"] * layers * args.steps / dt, 3),
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return 0
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    res = run_ours(args, rank, world, local)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

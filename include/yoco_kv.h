@@ -1,0 +1,193 @@
+/*
+ * yoco_kv.h — C ABI of the YOCO shared-KV cross-decoder hot path (GB300, sm_103a).
+ *
+ * A YOCO model computes one shared K^/V^ per token at the self-decoder
+ * boundary and caches it once; every cross-decoder layer then attends from
+ * its own queries to that one cache ("YOCO 论文与推理数据流详解", §3 and
+ * §10.3–§10.4). In a continuous-batching engine only the last scheduled
+ * token of each request has to enter the cross-decoder ("You Only Cache
+ * Once, in vLLM", "Implementation in vLLM"). The three calls below are that
+ * path: append the new K^/V^ into a paged cache, compact the batch to the
+ * cross-decoder rows, and run causal paged GQA attention for one layer.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Pointers named *device* are CUDA device pointers; the caller owns all
+ *    memory. The library never allocates, frees or synchronises a stream;
+ *    work is enqueued on `stream` (0 = legacy default stream).
+ *  - Host-detectable problems (null pointers, unsupported shapes, bad
+ *    alignment, too-small workspace) return a status before anything is
+ *    launched. A failed launch returns YOCO_ERR_CUDA.
+ *  - Data-dependent problems found on the device (a page id outside
+ *    [0, num_blocks), a position past the block table, a row with no key,
+ *    malformed offsets) never trap: the offending element is skipped and the
+ *    matching YOCO_DEVERR_* bit is OR-ed into `*err_word` (a device int32,
+ *    may be NULL). The caller clears it and reads it when it wants.
+ *  - Every call is asynchronous and makes no host<->device transfer, so a
+ *    sequence of calls can be captured in a CUDA graph.
+ *  - Cache layout ("KV cache memory systems", "Contiguous allocation wastes
+ *    capacity": logical token blocks map through a block table to
+ *    physical pages; the layout inside a page is not given there): two
+ *    pools k_cache / v_cache of shape [num_blocks][num_kv_heads][block_size]
+ *    [head_dim], row-major, so one (page, kv head) is one contiguous run of
+ *    block_size * head_dim elements. Token position p of request r is page
+ *    block_table[r * max_blocks_per_req + p / block_size], slot
+ *    p % block_size.
+ *  - Metadata names follow vLLM's CommonAttentionMetadata as shown in
+ *    "You Only Cache Once, in vLLM": query_start_loc [num_reqs + 1] holds
+ *    exclusive offsets of each request's scheduled tokens, seq_lens
+ *    [num_reqs] the tokens in the cache after this step (the scheduled
+ *    tokens included), block_table [num_reqs][max_blocks_per_req] int32.
+ *  - Supported shapes: head_dim in {64, 128, 256}; block_size in {16, 32};
+ *    num_q_heads a multiple of num_kv_heads with a group of at most 16;
+ *    dtype YOCO_F32 or YOCO_BF16 (attention accumulates in fp32 and writes
+ *    the input dtype).
+ *  - Preconditions the library cannot see: a step must not append into a
+ *    page another request still shares (prefix pages are copy-on-write,
+ *    "KV cache memory systems", "Prefix caching needs identity rules"); rows
+ *    skipped by the selection have no cross-decoder output, so a request
+ *    that wants prompt log-probabilities must not use it ("You Only Cache
+ *    Once, in vLLM", "Note").
+ */
+#ifndef YOCO_KV_H_
+#define YOCO_KV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    YOCO_OK = 0,
+    YOCO_ERR_INVALID_ARG = 1, /* null pointer, negative size, misaligned buffer, bad metadata shape */
+    YOCO_ERR_UNSUPPORTED = 2, /* head_dim / block_size / group / dtype outside the supported set */
+    YOCO_ERR_WORKSPACE = 3,   /* workspace pointer null or smaller than the size query returned */
+    YOCO_ERR_CUDA = 4         /* a CUDA runtime call or kernel launch failed */
+} yoco_status_t;
+
+typedef enum { YOCO_F32 = 0, YOCO_BF16 = 1 } yoco_dtype_t;
+
+/* Bits OR-ed into *err_word by device code. */
+#define YOCO_DEVERR_PAGE_RANGE 0x1   /* block_table entry outside [0, num_blocks) */
+#define YOCO_DEVERR_POS_RANGE 0x2    /* position beyond max_blocks_per_req * block_size, or negative */
+#define YOCO_DEVERR_EMPTY_ROW 0x4    /* a cross row with no key to attend (seq_len < rows of its request) */
+#define YOCO_DEVERR_OFFSETS 0x8      /* query_start_loc decreasing, or rows_per_req negative */
+#define YOCO_DEVERR_TIMEOUT 0x10     /* a bounded wait on an asynchronous copy gave up */
+
+/*
+ * yoco_kv_append — write the step's new shared K^/V^ into the paged cache.
+ *
+ * "YOCO 论文与推理数据流详解" §7.3 / §10.3: each token's K^/V^ is produced
+ * once at the self-decoder boundary and appended once to the single global
+ * cache (prefill appends the whole prompt, decode one position).
+ *
+ *   k_new, v_new      device, [num_tokens][num_kv_heads][head_dim], dtype; 16-byte aligned
+ *   k_cache, v_cache  device pools, layout above; 16-byte aligned
+ *   block_table       device int32 [num_reqs][max_blocks_per_req]
+ *   seq_lens          device int32 [num_reqs]
+ *   query_start_loc   device int32 [num_reqs + 1]; query_start_loc[num_reqs] must equal num_tokens
+ *   err_word          device int32 or NULL
+ * Token j of request r (0 <= j < q_len, q_len = qsl[r+1] - qsl[r]) goes to
+ * position seq_lens[r] - q_len + j. Results are bit-exact copies.
+ */
+yoco_status_t yoco_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                             const int32_t* block_table, int32_t max_blocks_per_req,
+                             const int32_t* seq_lens, const int32_t* query_start_loc,
+                             int32_t num_reqs, int32_t num_tokens, int32_t num_blocks,
+                             int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                             yoco_dtype_t dtype, int32_t* err_word, void* stream);
+
+/*
+ * yoco_select_cross_rows — compact a mixed prefill/decode batch to the
+ * cross-decoder rows.
+ *
+ * "You Only Cache Once, in vLLM", "Implementation in vLLM": the cross-decoder
+ * only needs the last prompt token of a prefilling request and every decode
+ * token; its metadata builder ("Adding torch.compile and cudagraph support")
+ * gives each request k_r rows, a new query_start_loc = running sum of k_r,
+ * and keeps seq_lens and the block table unchanged.
+ *
+ *   query_start_loc        device int32 [num_reqs + 1]
+ *   rows_per_req           device int32 [num_reqs] or NULL (= 1 per request);
+ *                          k_r = min(rows_per_req[r], q_len_r)
+ *   row_indices            device int32 out, capacity >= sum of k_r (<= num_tokens);
+ *                          row_indices[cqsl[r] + i] = qsl[r+1] - k_r + i
+ *   cross_query_start_loc  device int32 out [num_reqs + 1]
+ *   num_rows               device int32 out [1] (= cross_query_start_loc[num_reqs])
+ *   err_word               device int32 or NULL
+ * Bit-exact. num_reqs may be 0. Runs as one CTA; no host synchronisation.
+ */
+yoco_status_t yoco_select_cross_rows(const int32_t* query_start_loc, const int32_t* rows_per_req,
+                                     int32_t num_reqs, int32_t* row_indices,
+                                     int32_t* cross_query_start_loc, int32_t* num_rows,
+                                     int32_t* err_word, void* stream);
+
+/*
+ * yoco_cross_attn_workspace_size — bytes of fp32 scratch that
+ * yoco_cross_attn_paged needs for these bounds on the current device (the
+ * split-KV partial outputs and their log-sum-exp statistics). Returns 0 for
+ * unsupported or invalid arguments.
+ */
+size_t yoco_cross_attn_workspace_size(int32_t max_rows, int32_t num_q_heads, int32_t num_kv_heads,
+                                      int32_t head_dim, int32_t block_size, int32_t max_seq_len,
+                                      yoco_dtype_t dtype);
+
+/*
+ * yoco_cross_attn_paged — one cross-decoder layer's causal paged GQA attention.
+ *
+ * "KV cache memory systems", "Cache contents": out = softmax(q K^T / sqrt(d_h)) V
+ * over the cached keys up to the query position; "YOCO 论文与推理数据流详解"
+ * §10.4 / §11: each of the L/2 cross-decoder layers queries the same shared
+ * cache with its own Q, so this call runs once per layer over one cache.
+ * Row i of the k_r rows of request r attends to seq_lens[r] - k_r + i + 1
+ * keys (bottom-right causal, the query's own position included). Query head
+ * h reads kv head h / (num_q_heads / num_kv_heads).
+ *
+ *   q, out                 device [max_rows][num_q_heads][head_dim], dtype; rows beyond
+ *                          cross_query_start_loc[num_reqs] are neither read nor written
+ *   k_cache, v_cache       device pools (layout above), dtype
+ *   block_table, seq_lens  device int32, as for yoco_kv_append
+ *   cross_query_start_loc  device int32 [num_reqs + 1] (from yoco_select_cross_rows)
+ *   max_rows               host bound on the number of rows (grid size)
+ *   max_seq_len            host bound on seq_lens (sizes the split-KV grid)
+ *   scale                  softmax scale (1/sqrt(head_dim) for the pages' definition)
+ *   workspace              device scratch of >= yoco_cross_attn_workspace_size(...) bytes,
+ *                          16-byte aligned; contents need no initialisation
+ *   err_word               device int32 or NULL
+ * Long contexts are split across CTAs and merged with a log-sum-exp
+ * combine in a fixed split order, so results do not depend on where pages
+ * sit in the pool. Accuracy: fp32 accumulation; bf16 probabilities feed the
+ * tensor-core P.V product.
+ */
+yoco_status_t yoco_cross_attn_paged(const void* q, const void* k_cache, const void* v_cache,
+                                    void* out, const int32_t* block_table,
+                                    int32_t max_blocks_per_req, const int32_t* seq_lens,
+                                    const int32_t* cross_query_start_loc, int32_t num_reqs,
+                                    int32_t max_rows, int32_t max_seq_len, int32_t num_q_heads,
+                                    int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                    int32_t num_blocks, float scale, yoco_dtype_t dtype,
+                                    void* workspace, size_t workspace_bytes, int32_t* err_word,
+                                    void* stream);
+
+/*
+ * yoco_set_l2_window — mark [base, base + bytes) as persisting in L2 for
+ * work later enqueued on `stream` (bytes == 0 clears the window). The L2
+ * set-aside is a property of this process's CUDA context only. Used to
+ * keep a shared cache resident across the serial cross-decoder layers,
+ * which re-read it one after another ("YOCO 论文与推理数据流详解" §11).
+ */
+yoco_status_t yoco_set_l2_window(void* stream, void* base, size_t bytes, float hit_ratio);
+
+/* Human-readable name of a status code (static string). */
+const char* yoco_status_string(yoco_status_t status);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+int32_t yoco_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* YOCO_KV_H_ */

@@ -1,0 +1,58 @@
+"""The five workloads at full size, in the launch configuration the benchmark
+times: append and selection compared bit-exactly (whole pools), attention on
+sampled rows and layers against the oracle, plus properties that hold at any
+size."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.helpers import ATOL, gpu_out, oracle_bits, oracle_pools, oracle_step_out, pool_bits
+from workloads import FULL
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def P():
+    from yoco_shared_kv_gb300 import build
+    build.build()
+    from yoco_shared_kv_gb300 import pipeline
+    return pipeline
+
+
+@pytest.mark.parametrize("idx", [1, 2, 3, 4])
+def test_full_size(P, idx):
+    wl = FULL[idx]()
+    dw = P.DeviceWorkload(wl)
+    dw.run_fill()
+    dw.run_step(0)
+    torch.cuda.synchronize()
+    assert dw.error_bits() == 0
+    step = wl.steps[0]
+    ds = dw.steps[0]
+    # selection: bit-exact
+    o_rows, o_cq, n = oracle.select_cross_rows(step.query_start_loc, step.rows_per_req)
+    assert int(ds.num_rows.item()) == n == step.rows_upper
+    assert np.array_equal(ds.row_indices.cpu().numpy()[:n], o_rows)
+    assert np.array_equal(ds.cqsl.cpu().numpy(), o_cq)
+    # append: the whole pool, bit-exact (written slots and untouched sentinel)
+    kp, vp = oracle_pools(wl)
+    assert np.array_equal(pool_bits(dw.k_cache), oracle_bits(kp))
+    assert np.array_equal(pool_bits(dw.v_cache), oracle_bits(vp))
+    del kp, vp
+    # attention: every output finite; sampled rows x layers against the oracle
+    got = gpu_out(ds.out)
+    assert np.isfinite(got).all()
+    rng = np.random.default_rng(idx)
+    rows = sorted(set([0, n - 1] + rng.choice(n, size=min(n, 3), replace=False).tolist()))
+    layers = [0, wl.layers - 1]
+    ref = oracle_step_out(wl, step, layers=layers, rows=rows)
+    sub = got[layers][:, rows]
+    err = np.abs(sub - ref).max()
+    assert err <= ATOL[wl.dtype], (wl.name, err)
+    # layers differ only through their queries: re-running a layer reproduces it exactly
+    again = torch.empty_like(ds.out[0])
+    dw.attend(ds, 0, out=again)
+    torch.cuda.synchronize()
+    assert torch.equal(again.view(torch.int16), ds.out[0].view(torch.int16))

@@ -1,0 +1,256 @@
+"""GPU path vs the CPU oracle, element by element (bit-exact for append and
+selection; max-abs tolerance for attention), through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.helpers import (ATOL, gpu_out, oracle_bits, oracle_pools, oracle_step_out, pool_bits)
+from workloads import SMALL, Workload, pure_decode
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def N():
+    from yoco_shared_kv_gb300 import build
+    build.build()
+    from yoco_shared_kv_gb300 import _native
+    return _native
+
+
+@pytest.fixture(scope="module")
+def P(N):
+    from yoco_shared_kv_gb300 import pipeline
+    return pipeline
+
+
+def _i32(x):
+    return torch.tensor(np.asarray(x, dtype=np.int32), device="cuda")
+
+
+# ------------------------------------------------------------------ selection
+
+
+def _gpu_select(N, qsl, rpr=None, cap=None):
+    qsl = np.asarray(qsl, dtype=np.int32)
+    R = len(qsl) - 1
+    cap = cap or max(int(qsl[-1]) if R else 0, 1) + 64
+    rows = torch.full((cap,), -7, dtype=torch.int32, device="cuda")
+    cq = torch.full((R + 1,), -7, dtype=torch.int32, device="cuda")
+    nr = torch.full((1,), -7, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    N.yoco_select_cross_rows(_i32(qsl), None if rpr is None else _i32(rpr), rows, cq, nr, err)
+    torch.cuda.synchronize()
+    n = int(nr.item())
+    return rows.cpu().numpy(), cq.cpu().numpy(), n, int(err.item())
+
+
+def test_select_worked_example(N, golden_dir):
+    import json, os
+    g = json.load(open(os.path.join(golden_dir, "select_vllm_example.json")))
+    rows, cq, n, err = _gpu_select(N, g["query_start_loc"], g["rows_per_req"])
+    assert err == 0 and n == 4
+    assert rows[:n].tolist() == g["expected_rows"]
+    assert cq.tolist() == g["expected_cross_query_start_loc"]
+    assert (rows[n:] == -7).all()  # nothing written past the rows
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_select_random_bit_exact(N, seed):
+    rng = np.random.default_rng(100 + seed)
+    R = int(rng.choice([1, 7, 33, 1023, 1024, 1025, 3000, 5000]))
+    qlen = rng.integers(0, 12, size=R)
+    qlen[rng.random(R) < 0.6] = 1
+    qsl = np.concatenate([[0], np.cumsum(qlen)]).astype(np.int32)
+    rpr = None if seed % 3 == 0 else rng.integers(0, 6, size=R).astype(np.int32)
+    rows, cq, n, err = _gpu_select(N, qsl, rpr)
+    o_rows, o_cq, o_n = oracle.select_cross_rows(qsl, rpr)
+    assert err == 0 and n == o_n
+    assert np.array_equal(rows[:n], o_rows)
+    assert np.array_equal(cq, o_cq)
+
+
+def test_select_edge_cases(N):
+    rows, cq, n, err = _gpu_select(N, [0])
+    assert n == 0 and cq.tolist() == [0] and err == 0
+    rows, cq, n, err = _gpu_select(N, [0, 0, 3, 3])
+    assert n == 1 and rows[0] == 2 and cq.tolist() == [0, 0, 1, 1]
+    rows, cq, n, err = _gpu_select(N, [0, 2, 5], [7, 0])
+    assert n == 2 and rows[:2].tolist() == [0, 1] and cq.tolist() == [0, 2, 2]
+    _, _, _, err = _gpu_select(N, [0, 3, 2])
+    assert err & N.DEVERR_OFFSETS
+
+
+# --------------------------------------------------------------------- append
+
+
+@pytest.mark.parametrize("idx", [0, 1, 2, 3, 4])
+def test_append_bit_exact_whole_pool(P, idx):
+    wl = SMALL[idx]()
+    dw = P.DeviceWorkload(wl)
+    dw.run_fill()
+    for i in range(len(dw.steps)):
+        dw.append(dw.steps[i])
+    torch.cuda.synchronize()
+    assert dw.error_bits() == 0
+    kp, vp = oracle_pools(wl)
+    assert np.array_equal(pool_bits(dw.k_cache), oracle_bits(kp))
+    assert np.array_equal(pool_bits(dw.v_cache), oracle_bits(vp))
+
+
+def test_append_bad_page_sets_error_and_skips(P, N):
+    wl = SMALL[1]()
+    dw = P.DeviceWorkload(wl)
+    ds = dw.steps[0]
+    bt = ds.dev["block_table"].clone()
+    bt[0, :] = wl.num_blocks + 5  # request 0 points past the pool
+    N.yoco_kv_append(ds.dev["k_new"], ds.dev["v_new"], dw.k_cache, dw.v_cache, bt,
+                     ds.dev["seq_lens"], ds.dev["qsl"], dw.err)
+    torch.cuda.synchronize()
+    assert dw.error_bits() & N.DEVERR_PAGE_RANGE
+    # everything else was still written, exactly as the oracle skips it
+    step = wl.steps[0]
+    kp, vp = wl.empty_pool(), wl.empty_pool()
+    bad_bt = step.block_table.copy()
+    bad_bt[0, :] = wl.num_blocks + 5
+    skipped = oracle.kv_append(step.k_new, step.v_new, kp, vp, bad_bt, step.seq_lens,
+                               step.query_start_loc, wl.block_size)
+    assert skipped == wl.num_kv_heads
+    assert np.array_equal(pool_bits(dw.k_cache), oracle_bits(kp))
+
+
+# ------------------------------------------------------------------ attention
+
+
+@pytest.mark.parametrize("idx", [0, 1, 2, 3, 4])
+def test_step_matches_oracle(P, idx):
+    """Fill + every step (append -> select -> all layers) vs the oracle, every output."""
+    wl = SMALL[idx]()
+    dw = P.DeviceWorkload(wl)
+    dw.run_fill()
+    for i, step in enumerate(wl.steps):
+        dw.run_step(i)
+        torch.cuda.synchronize()
+        assert dw.error_bits() == 0
+        ds = dw.steps[i]
+        o_rows, o_cq, n = oracle.select_cross_rows(step.query_start_loc, step.rows_per_req)
+        assert int(ds.num_rows.item()) == n
+        assert np.array_equal(ds.row_indices.cpu().numpy()[:n], o_rows)
+        assert np.array_equal(ds.cqsl.cpu().numpy(), o_cq)
+        ref = oracle_step_out(wl, step)
+        got = gpu_out(ds.out)
+        assert np.isfinite(got).all()
+        err = np.abs(got - ref).max()
+        assert err <= ATOL[wl.dtype], (wl.name, i, err)
+
+
+def test_attention_page_permutation_bit_identical(P):
+    a = SMALL[1]()
+    b = SMALL[1]()
+    perm = np.random.default_rng(11).permutation(b.num_blocks).astype(np.int32)
+    for st in [b.fill] + b.steps:
+        st.block_table = perm[st.block_table]
+    outs = []
+    for wl in (a, b):
+        dw = P.DeviceWorkload(wl)
+        dw.run_all()
+        torch.cuda.synchronize()
+        assert dw.error_bits() == 0
+        outs.append(dw.steps[0].out.cpu())
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+
+
+def test_attention_single_key_and_block_edges(P):
+    """Contexts of 1, block_size, block_size + 1 tokens (and a long one) in one batch."""
+    wl = pure_decode(3001, explicit_lens=[1, 16, 17, 32, 33, 2049], layers=2)
+    dw = P.DeviceWorkload(wl)
+    dw.run_all()
+    torch.cuda.synchronize()
+    assert dw.error_bits() == 0
+    got = gpu_out(dw.steps[0].out)
+    ref = oracle_step_out(wl, wl.steps[0])
+    assert np.abs(got - ref).max() <= ATOL["bf16"]
+    # a single key returns V exactly (bf16 rounding of an exactly representable value)
+    K, V = wl.request_kv(0)
+    v0 = oracle.widen(V[0], "bf16")  # [H_kv, D]
+    G = wl.num_q_heads // wl.num_kv_heads
+    for h in range(wl.num_q_heads):
+        assert np.array_equal(got[0, 0, h], v0[h // G])
+
+
+@pytest.mark.parametrize("H_q,H_kv,D,bs", [(4, 4, 64, 16), (6, 2, 128, 32), (12, 1, 64, 32),
+                                           (16, 2, 256, 16), (2, 1, 128, 16), (16, 16, 128, 32)])
+def test_attention_shapes(P, H_q, H_kv, D, bs):
+    wl = pure_decode(4000 + H_q * 7 + D, num_reqs=5, ctx_lo=1, ctx_hi=900, H_q=H_q, H_kv=H_kv,
+                     D=D, bs=bs, layers=2)
+    dw = P.DeviceWorkload(wl)
+    dw.run_all()
+    torch.cuda.synchronize()
+    assert dw.error_bits() == 0
+    got = gpu_out(dw.steps[0].out)
+    ref = oracle_step_out(wl, wl.steps[0])
+    assert np.abs(got - ref).max() <= ATOL["bf16"]
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_attention_fp32_shapes(P, D):
+    wl = pure_decode(5000 + D, num_reqs=4, ctx_lo=1, ctx_hi=700, H_q=8, H_kv=2, D=D, bs=16,
+                     layers=2, dtype="f32")
+    dw = P.DeviceWorkload(wl)
+    dw.run_all()
+    torch.cuda.synchronize()
+    assert dw.error_bits() == 0
+    got = gpu_out(dw.steps[0].out)
+    ref = oracle_step_out(wl, wl.steps[0])
+    assert np.abs(got - ref).max() <= ATOL["f32"]
+
+
+def test_multi_row_requests_bottom_right_causal(P):
+    """rows_per_req > 1: trailing rows of a prefill see their own causal prefix."""
+    from workloads import mixed_step
+    wl = mixed_step(6001, n_decode=3, dec_lo=50, dec_hi=300, n_prefill=3, pre_lo=20, pre_hi=200,
+                    layers=2, rows_per_req=[1, 1, 1, 4, 2, 7])
+    dw = P.DeviceWorkload(wl)
+    dw.run_all()
+    torch.cuda.synchronize()
+    assert dw.error_bits() == 0
+    got = gpu_out(dw.steps[0].out)
+    ref = oracle_step_out(wl, wl.steps[0])
+    assert np.abs(got - ref).max() <= ATOL["bf16"]
+
+
+def test_attention_empty_row_and_bad_page_flagged(P, N):
+    wl = SMALL[1]()
+    dw = P.DeviceWorkload(wl)
+    dw.run_all()
+    ds = dw.steps[0]
+    # seq_len 0 for request 0: its row has no key -> zero output + flag
+    sl = ds.dev["seq_lens"].clone()
+    sl[0] = 0
+    out = torch.full_like(ds.out[0], 3.0)
+    dw.err.zero_()
+    N.yoco_cross_attn_paged(ds.dev["q"][0], dw.k_cache, dw.v_cache, out, ds.dev["block_table"],
+                            sl, ds.cqsl, ds.max_seq_len, wl.scale, ds.workspace, dw.err)
+    torch.cuda.synchronize()
+    assert dw.error_bits() & N.DEVERR_EMPTY_ROW
+    assert (out[0] == 0).all()
+    # a page id past the pool: flagged, skipped, no fault
+    bt = ds.dev["block_table"].clone()
+    bt[3, 2] = -4
+    dw.err.zero_()
+    N.yoco_cross_attn_paged(ds.dev["q"][0], dw.k_cache, dw.v_cache, out, bt, ds.dev["seq_lens"],
+                            ds.cqsl, ds.max_seq_len, wl.scale, ds.workspace, dw.err)
+    torch.cuda.synchronize()
+    assert dw.error_bits() & N.DEVERR_PAGE_RANGE
+
+
+def test_workspace_too_small_is_rejected(P, N):
+    wl = SMALL[3]()
+    dw = P.DeviceWorkload(wl)
+    ds = dw.steps[0]
+    with pytest.raises(N.YocoError) as e:
+        N.yoco_cross_attn_paged(ds.dev["q"][0], dw.k_cache, dw.v_cache, ds.out[0],
+                                ds.dev["block_table"], ds.dev["seq_lens"], ds.cqsl, 131072,
+                                wl.scale, ds.workspace[:16], dw.err)
+    assert e.value.status == N.YOCO_ERR_WORKSPACE

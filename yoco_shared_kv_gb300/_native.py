@@ -1,0 +1,174 @@
+"""ctypes binding of ``include/yoco_kv.h`` — argument marshalling only.
+
+Every function here has the name of the C entry point it wraps, takes torch
+tensors that already live on the GPU, checks their dtype/shape/contiguity,
+and passes raw pointers and sizes through. All arithmetic happens in the
+CUDA library. There is no fallback: if the library is not built, importing
+this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libyoco_kv.so")
+
+YOCO_OK, YOCO_ERR_INVALID_ARG, YOCO_ERR_UNSUPPORTED, YOCO_ERR_WORKSPACE, YOCO_ERR_CUDA = range(5)
+YOCO_F32, YOCO_BF16 = 0, 1
+DEVERR_PAGE_RANGE = 0x1
+DEVERR_POS_RANGE = 0x2
+DEVERR_EMPTY_ROW = 0x4
+DEVERR_OFFSETS = 0x8
+DEVERR_TIMEOUT = 0x10
+
+EXPORTED = ("yoco_kv_append", "yoco_select_cross_rows", "yoco_cross_attn_workspace_size",
+            "yoco_cross_attn_paged", "yoco_set_l2_window", "yoco_status_string", "yoco_version")
+
+
+class YocoError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {status_name(status)} (status {status})")
+        self.status = status
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"CUDA library not built: {LIB_PATH} is missing "
+                          "(run yoco_shared_kv_gb300.build.build())")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    L.yoco_kv_append.restype = ctypes.c_int
+    L.yoco_kv_append.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32,
+                                 ctypes.c_int, vp, vp]
+    L.yoco_select_cross_rows.restype = ctypes.c_int
+    L.yoco_select_cross_rows.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp]
+    L.yoco_cross_attn_workspace_size.restype = sz
+    L.yoco_cross_attn_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.c_int]
+    L.yoco_cross_attn_paged.restype = ctypes.c_int
+    L.yoco_cross_attn_paged.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32,
+                                        i32, i32, i32, ctypes.c_float, ctypes.c_int, vp, sz, vp, vp]
+    L.yoco_set_l2_window.restype = ctypes.c_int
+    L.yoco_set_l2_window.argtypes = [vp, vp, sz, ctypes.c_float]
+    L.yoco_status_string.restype = ctypes.c_char_p
+    L.yoco_status_string.argtypes = [ctypes.c_int]
+    L.yoco_version.restype = ctypes.c_int32
+    L.yoco_version.argtypes = []
+    return L
+
+
+lib = _load()
+
+
+def status_name(status: int) -> str:
+    return lib.yoco_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int) -> None:
+    if status != YOCO_OK:
+        raise YocoError(fn, status)
+
+
+def dtype_code(t: torch.dtype) -> int:
+    if t == torch.bfloat16:
+        return YOCO_BF16
+    if t == torch.float32:
+        return YOCO_F32
+    raise ValueError(f"unsupported dtype {t}")
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _i32(t: torch.Tensor, name: str) -> int:
+    if t.dtype != torch.int32:
+        raise ValueError(f"{name} must be int32")
+    return _ptr(t)
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def yoco_kv_append(k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+                   v_cache: torch.Tensor, block_table: torch.Tensor, seq_lens: torch.Tensor,
+                   query_start_loc: torch.Tensor, err_word: Optional[torch.Tensor] = None,
+                   stream=None) -> None:
+    """Append ``k_new/v_new [T, H_kv, D]`` into pools ``[num_blocks, H_kv, bs, D]``."""
+    num_blocks, H_kv, bs, D = k_cache.shape
+    assert v_cache.shape == k_cache.shape and k_new.shape == v_new.shape
+    assert k_new.dtype == k_cache.dtype == v_cache.dtype == v_new.dtype
+    T = k_new.shape[0]
+    assert k_new.shape[1:] == (H_kv, D)
+    R = query_start_loc.shape[0] - 1
+    _check("yoco_kv_append", lib.yoco_kv_append(
+        _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _i32(block_table, "block_table"),
+        block_table.shape[1], _i32(seq_lens, "seq_lens"), _i32(query_start_loc, "query_start_loc"),
+        R, T, num_blocks, bs, H_kv, D, dtype_code(k_cache.dtype),
+        None if err_word is None else _i32(err_word, "err_word"), _stream(stream)))
+
+
+def yoco_select_cross_rows(query_start_loc: torch.Tensor, rows_per_req: Optional[torch.Tensor],
+                           row_indices: torch.Tensor, cross_query_start_loc: torch.Tensor,
+                           num_rows: torch.Tensor, err_word: Optional[torch.Tensor] = None,
+                           stream=None) -> None:
+    R = query_start_loc.shape[0] - 1
+    assert cross_query_start_loc.shape[0] == R + 1
+    _check("yoco_select_cross_rows", lib.yoco_select_cross_rows(
+        _i32(query_start_loc, "query_start_loc"),
+        None if rows_per_req is None else _i32(rows_per_req, "rows_per_req"), R,
+        _i32(row_indices, "row_indices"), _i32(cross_query_start_loc, "cross_query_start_loc"),
+        _i32(num_rows, "num_rows"), None if err_word is None else _i32(err_word, "err_word"),
+        _stream(stream)))
+
+
+def yoco_cross_attn_workspace_size(max_rows: int, num_q_heads: int, num_kv_heads: int,
+                                   head_dim: int, block_size: int, max_seq_len: int,
+                                   dtype: torch.dtype) -> int:
+    return int(lib.yoco_cross_attn_workspace_size(max_rows, num_q_heads, num_kv_heads, head_dim,
+                                                  block_size, max_seq_len, dtype_code(dtype)))
+
+
+def yoco_cross_attn_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                          out: torch.Tensor, block_table: torch.Tensor, seq_lens: torch.Tensor,
+                          cross_query_start_loc: torch.Tensor, max_seq_len: int, scale: float,
+                          workspace: Optional[torch.Tensor], err_word: Optional[torch.Tensor] = None,
+                          stream=None, max_rows: Optional[int] = None) -> None:
+    """One layer: ``q/out [max_rows, H_q, D]`` against pools ``[num_blocks, H_kv, bs, D]``."""
+    num_blocks, H_kv, bs, D = k_cache.shape
+    rows_cap, H_q, Dq = q.shape
+    assert Dq == D and out.shape == q.shape and out.dtype == q.dtype == k_cache.dtype
+    R = cross_query_start_loc.shape[0] - 1
+    max_rows = rows_cap if max_rows is None else max_rows
+    assert max_rows <= rows_cap
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("yoco_cross_attn_paged", lib.yoco_cross_attn_paged(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _i32(block_table, "block_table"),
+        block_table.shape[1], _i32(seq_lens, "seq_lens"),
+        _i32(cross_query_start_loc, "cross_query_start_loc"), R, max_rows, int(max_seq_len), H_q,
+        H_kv, D, bs, num_blocks, float(scale), dtype_code(q.dtype), _ptr(workspace), ws_bytes,
+        None if err_word is None else _i32(err_word, "err_word"), _stream(stream)))
+
+
+def yoco_set_l2_window(base: Optional[torch.Tensor], nbytes: int, hit_ratio: float = 1.0,
+                       stream=None) -> None:
+    _check("yoco_set_l2_window", lib.yoco_set_l2_window(
+        _stream(stream), None if base is None else base.data_ptr(), int(nbytes), float(hit_ratio)))
+
+
+def yoco_version() -> int:
+    return int(lib.yoco_version())

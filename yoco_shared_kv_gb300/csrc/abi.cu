@@ -1,0 +1,50 @@
+// Library-wide C entry points: status strings, version, L2 persistence window.
+#include "common.cuh"
+
+extern "C" const char* yoco_status_string(yoco_status_t status) {
+    switch (status) {
+        case YOCO_OK: return "ok";
+        case YOCO_ERR_INVALID_ARG: return "invalid argument";
+        case YOCO_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case YOCO_ERR_WORKSPACE: return "workspace missing or too small";
+        case YOCO_ERR_CUDA: return "CUDA runtime error";
+    }
+    return "unknown status";
+}
+
+extern "C" int32_t yoco_version(void) { return 100; }  // 0.1.0
+
+// The serial cross-decoder layers re-read one shared cache ("YOCO
+// 论文与推理数据流详解" §11); when the cache (or its hot part) fits in L2,
+// a persisting access-policy window keeps it there between layers.
+extern "C" yoco_status_t yoco_set_l2_window(void* stream, void* base, size_t bytes,
+                                            float hit_ratio) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaStreamAttrValue attr = {};
+    if (bytes == 0 || base == nullptr) {
+        attr.accessPolicyWindow.base_ptr = nullptr;
+        attr.accessPolicyWindow.num_bytes = 0;
+        attr.accessPolicyWindow.hitRatio = 0.f;
+        attr.accessPolicyWindow.hitProp = cudaAccessPropertyNormal;
+        attr.accessPolicyWindow.missProp = cudaAccessPropertyNormal;
+        YOCO_CUDA_OK(cudaStreamSetAttribute(s, cudaStreamAttributeAccessPolicyWindow, &attr));
+        return YOCO_OK;
+    }
+    if (!(hit_ratio >= 0.f && hit_ratio <= 1.f)) return YOCO_ERR_INVALID_ARG;
+    int dev = 0, max_win = 0, max_persist = 0;
+    YOCO_CUDA_OK(cudaGetDevice(&dev));
+    YOCO_CUDA_OK(cudaDeviceGetAttribute(&max_win, cudaDevAttrMaxAccessPolicyWindowSize, dev));
+    YOCO_CUDA_OK(cudaDeviceGetAttribute(&max_persist, cudaDevAttrMaxPersistingL2CacheSize, dev));
+    if (max_win <= 0 || max_persist <= 0) return YOCO_ERR_UNSUPPORTED;
+    const size_t win = bytes < static_cast<size_t>(max_win) ? bytes : static_cast<size_t>(max_win);
+    const size_t keep = win < static_cast<size_t>(max_persist) ? win : static_cast<size_t>(max_persist);
+    // the set-aside is a limit of this process's context only
+    YOCO_CUDA_OK(cudaDeviceSetLimit(cudaLimitPersistingL2CacheSize, keep));
+    attr.accessPolicyWindow.base_ptr = base;
+    attr.accessPolicyWindow.num_bytes = win;
+    attr.accessPolicyWindow.hitRatio = hit_ratio;
+    attr.accessPolicyWindow.hitProp = cudaAccessPropertyPersisting;
+    attr.accessPolicyWindow.missProp = cudaAccessPropertyStreaming;
+    YOCO_CUDA_OK(cudaStreamSetAttribute(s, cudaStreamAttributeAccessPolicyWindow, &attr));
+    return YOCO_OK;
+}

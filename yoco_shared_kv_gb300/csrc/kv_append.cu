@@ -1,0 +1,144 @@
+// yoco_kv_append: write a step's new shared K^/V^ rows into the paged cache.
+//
+// "YOCO 论文与推理数据流详解" §7.3 and §10.3: each token's K^/V^ is produced
+// once at the self-decoder boundary and appended once to the one global
+// cache. "KV cache memory systems", "Contiguous allocation wastes capacity":
+// a token's logical block resolves to a physical page through the block table.
+//
+// Design: one warp copies one (token, kv head) row of K and of V, 16 bytes
+// per lane per instruction (a head_dim row is 128..1024 bytes, so a warp
+// covers it in one or two vector loads and stores). The request of a token
+// is found by a binary search over query_start_loc; no host-side
+// slot_mapping is needed, so the call is graph-capturable.
+#include "common.cuh"
+
+namespace yoco {
+namespace {
+
+constexpr int kAppendWarps = 8;
+
+template <int ROW_VECS>  // 16-byte vectors per (token, head) row
+__global__ void __launch_bounds__(kAppendWarps * 32)
+    kv_append_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+                     uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                     const int32_t* __restrict__ block_table, int32_t max_blocks,
+                     const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ qsl,
+                     int32_t num_reqs, int32_t num_tokens, int32_t num_blocks, int32_t block_size,
+                     int32_t num_kv_heads, int32_t* err) {
+    const int lane = threadIdx.x & 31;
+    const int64_t total_rows = static_cast<int64_t>(num_tokens) * num_kv_heads;
+    const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * kAppendWarps + (threadIdx.x >> 5);
+    const int64_t wstride = static_cast<int64_t>(gridDim.x) * kAppendWarps;
+    const int32_t last = __ldg(qsl + num_reqs);
+    for (int64_t row = warp0; row < total_rows; row += wstride) {
+        const int32_t tok = static_cast<int32_t>(row / num_kv_heads);
+        const int32_t h = static_cast<int32_t>(row - static_cast<int64_t>(tok) * num_kv_heads);
+        if (tok >= last || __ldg(qsl) > tok) {  // token outside every request's range
+            if (lane == 0) set_err(err, YOCO_DEVERR_OFFSETS);
+            continue;
+        }
+        // first r with qsl[r + 1] > tok
+        int32_t lo = 0, hi = num_reqs - 1;
+        while (lo < hi) {
+            const int32_t mid = (lo + hi) >> 1;
+            if (__ldg(qsl + mid + 1) > tok) hi = mid;
+            else lo = mid + 1;
+        }
+        const int32_t q0 = __ldg(qsl + lo), q1 = __ldg(qsl + lo + 1);
+        const int32_t q_len = q1 - q0;
+        const int64_t pos = static_cast<int64_t>(__ldg(seq_lens + lo)) - q_len + (tok - q0);
+        if (q_len <= 0) {
+            if (lane == 0) set_err(err, YOCO_DEVERR_OFFSETS);
+            continue;
+        }
+        if (pos < 0 || pos / block_size >= max_blocks) {
+            if (lane == 0) set_err(err, YOCO_DEVERR_POS_RANGE);
+            continue;
+        }
+        const int32_t page =
+            __ldg(block_table + static_cast<int64_t>(lo) * max_blocks + pos / block_size);
+        if (page < 0 || page >= num_blocks) {
+            if (lane == 0) set_err(err, YOCO_DEVERR_PAGE_RANGE);
+            continue;
+        }
+        const int64_t dst =
+            ((static_cast<int64_t>(page) * num_kv_heads + h) * block_size + pos % block_size) *
+            ROW_VECS;
+        const int64_t src = row * ROW_VECS;
+#pragma unroll
+        for (int v = lane; v < ROW_VECS; v += 32) {
+            const uint4 kv = __ldcs(k_new + src + v);  // read once: stream past L1/L2
+            const uint4 vv = __ldcs(v_new + src + v);
+            k_cache[dst + v] = kv;
+            v_cache[dst + v] = vv;
+        }
+    }
+}
+
+template <int ROW_VECS>
+cudaError_t launch_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                          const int32_t* bt, int32_t max_blocks, const int32_t* seq_lens,
+                          const int32_t* qsl, int32_t num_reqs, int32_t num_tokens,
+                          int32_t num_blocks, int32_t bs, int32_t H_kv, int32_t* err,
+                          cudaStream_t s) {
+    const int64_t rows = static_cast<int64_t>(num_tokens) * H_kv;
+    int64_t blocks = (rows + kAppendWarps - 1) / kAppendWarps;
+    const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    kv_append_kernel<ROW_VECS><<<static_cast<unsigned>(blocks), kAppendWarps * 32, 0, s>>>(
+        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
+        static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), bt, max_blocks, seq_lens, qsl,
+        num_reqs, num_tokens, num_blocks, bs, H_kv, err);
+    return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace yoco
+
+extern "C" yoco_status_t yoco_kv_append(const void* k_new, const void* v_new, void* k_cache,
+                                        void* v_cache, const int32_t* block_table,
+                                        int32_t max_blocks_per_req, const int32_t* seq_lens,
+                                        const int32_t* query_start_loc, int32_t num_reqs,
+                                        int32_t num_tokens, int32_t num_blocks,
+                                        int32_t block_size, int32_t num_kv_heads,
+                                        int32_t head_dim, yoco_dtype_t dtype, int32_t* err_word,
+                                        void* stream) {
+    using namespace yoco;
+    if (!dtype_ok(dtype)) return YOCO_ERR_UNSUPPORTED;
+    if (!head_dim_ok(head_dim) || !block_size_ok(block_size)) return YOCO_ERR_UNSUPPORTED;
+    if (num_reqs < 0 || num_tokens < 0 || num_blocks <= 0 || num_kv_heads <= 0 ||
+        max_blocks_per_req <= 0)
+        return YOCO_ERR_INVALID_ARG;
+    if (num_tokens == 0 || num_reqs == 0) return YOCO_OK;
+    if (!k_new || !v_new || !k_cache || !v_cache || !block_table || !seq_lens || !query_start_loc)
+        return YOCO_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+        return YOCO_ERR_INVALID_ARG;
+    const int vecs = static_cast<int>(head_dim * elem_size(dtype) / 16);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    switch (vecs) {
+        case 8: e = launch_append<8>(k_new, v_new, k_cache, v_cache, block_table,
+                                     max_blocks_per_req, seq_lens, query_start_loc, num_reqs,
+                                     num_tokens, num_blocks, block_size, num_kv_heads, err_word, s);
+            break;
+        case 16: e = launch_append<16>(k_new, v_new, k_cache, v_cache, block_table,
+                                       max_blocks_per_req, seq_lens, query_start_loc, num_reqs,
+                                       num_tokens, num_blocks, block_size, num_kv_heads, err_word,
+                                       s);
+            break;
+        case 32: e = launch_append<32>(k_new, v_new, k_cache, v_cache, block_table,
+                                       max_blocks_per_req, seq_lens, query_start_loc, num_reqs,
+                                       num_tokens, num_blocks, block_size, num_kv_heads, err_word,
+                                       s);
+            break;
+        case 64: e = launch_append<64>(k_new, v_new, k_cache, v_cache, block_table,
+                                       max_blocks_per_req, seq_lens, query_start_loc, num_reqs,
+                                       num_tokens, num_blocks, block_size, num_kv_heads, err_word,
+                                       s);
+            break;
+        default: return YOCO_ERR_UNSUPPORTED;
+    }
+    return e == cudaSuccess ? YOCO_OK : YOCO_ERR_CUDA;
+}

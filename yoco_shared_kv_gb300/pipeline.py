@@ -1,0 +1,140 @@
+"""One scheduling step of the cross-decoder hot path on the GPU.
+
+``DeviceWorkload`` holds a workload's buffers in device memory (the paged
+K^/V^ pools, metadata, per-layer queries and outputs) and runs the path:
+
+    yoco_kv_append          (shared K^/V^ of the step's tokens, once)
+    yoco_select_cross_rows  (rows entering the cross-decoder)
+    yoco_cross_attn_paged   x layers (each layer's own queries, same cache)
+
+as in "YOCO 论文与推理数据流详解" §13.4 (self-prefill, global-KV finalize,
+cross-decode) and "You Only Cache Once, in vLLM" (cross-decoder batch =
+one row per scheduled request). Only allocation and argument marshalling
+happen here; every step of the path runs in the CUDA library.
+"""
+from __future__ import annotations
+
+from typing import List, Optional
+
+import numpy as np
+import torch
+
+from . import _native as N
+
+
+def to_torch(arr: np.ndarray, dtype: str) -> torch.Tensor:
+    """Storage-dtype numpy array -> CPU torch tensor sharing its bits."""
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(arr).view(np.int16)).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(arr, dtype=np.float32))
+
+
+def torch_dtype(dtype: str) -> torch.dtype:
+    return {"bf16": torch.bfloat16, "f32": torch.float32}[dtype]
+
+
+class DeviceStep:
+    """Device copies of one step's inputs, plus its outputs and scratch."""
+
+    def __init__(self, wl, step, device, pin_host: bool = False):
+        self.wl, self.step = wl, step
+        dev = torch.device(device)
+        i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32))  # noqa: E731
+        host = {
+            "qsl": i32(step.query_start_loc),
+            "seq_lens": i32(step.seq_lens),
+            "block_table": i32(step.block_table),
+            "k_new": to_torch(step.k_new, wl.dtype),
+            "v_new": to_torch(step.v_new, wl.dtype),
+        }
+        if step.rows_per_req is not None:
+            host["rows_per_req"] = i32(step.rows_per_req)
+        if step.q is not None:
+            host["q"] = to_torch(step.q, wl.dtype)
+        if pin_host:
+            host = {k: v.pin_memory() for k, v in host.items()}
+        self.host = host
+        self.dev = {k: v.to(dev) for k, v in host.items()}
+        R, T = step.num_reqs, step.num_tokens
+        self.num_reqs, self.num_tokens = R, T
+        self.max_seq_len = int(step.seq_lens.max()) if R else 1
+        self.rows_upper = step.rows_upper
+        self.row_indices = torch.zeros(max(T, 1), dtype=torch.int32, device=dev)
+        self.cqsl = torch.zeros(R + 1, dtype=torch.int32, device=dev)
+        self.num_rows = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.out = None
+        self.workspace = None
+        if step.q is not None:
+            self.out = torch.empty_like(self.dev["q"])
+            ws = N.yoco_cross_attn_workspace_size(max(self.rows_upper, 1), wl.num_q_heads,
+                                                  wl.num_kv_heads, wl.head_dim, wl.block_size,
+                                                  self.max_seq_len, torch_dtype(wl.dtype))
+            self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+
+    def h2d(self, stream=None) -> int:
+        """Re-copy the step's inputs from (pinned) host memory; returns bytes copied."""
+        nbytes = 0
+        for k, v in self.host.items():
+            self.dev[k].copy_(v, non_blocking=True)
+            nbytes += v.numel() * v.element_size()
+        return nbytes
+
+
+class DeviceWorkload:
+    def __init__(self, wl, device="cuda", pin_host: bool = False, sentinel: bool = True):
+        self.wl = wl
+        self.device = torch.device(device)
+        tdt = torch_dtype(wl.dtype)
+        shape = wl.pool_shape()
+        if sentinel:
+            # all-ones bytes: NaN in both dtypes, so a stray read poisons the output
+            self.k_cache = torch.full(shape, -1, dtype=torch.int16 if tdt == torch.bfloat16
+                                      else torch.int32, device=self.device).view(tdt)
+            self.v_cache = torch.full(shape, -1, dtype=torch.int16 if tdt == torch.bfloat16
+                                      else torch.int32, device=self.device).view(tdt)
+        else:
+            self.k_cache = torch.empty(shape, dtype=tdt, device=self.device)
+            self.v_cache = torch.empty(shape, dtype=tdt, device=self.device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self.fill = DeviceStep(wl, wl.fill, device, pin_host) if wl.fill is not None else None
+        self.steps: List[DeviceStep] = [DeviceStep(wl, s, device, pin_host) for s in wl.steps]
+
+    # ------------------------------------------------------------------ calls
+
+    def append(self, ds: DeviceStep, stream=None) -> None:
+        d = ds.dev
+        N.yoco_kv_append(d["k_new"], d["v_new"], self.k_cache, self.v_cache, d["block_table"],
+                         d["seq_lens"], d["qsl"], self.err, stream)
+
+    def select(self, ds: DeviceStep, stream=None) -> None:
+        d = ds.dev
+        N.yoco_select_cross_rows(d["qsl"], d.get("rows_per_req"), ds.row_indices, ds.cqsl,
+                                 ds.num_rows, self.err, stream)
+
+    def attend(self, ds: DeviceStep, layer: int, stream=None, q: Optional[torch.Tensor] = None,
+               out: Optional[torch.Tensor] = None) -> None:
+        d = ds.dev
+        N.yoco_cross_attn_paged(d["q"][layer] if q is None else q, self.k_cache, self.v_cache,
+                                ds.out[layer] if out is None else out, d["block_table"],
+                                d["seq_lens"], ds.cqsl, ds.max_seq_len, self.wl.scale,
+                                ds.workspace, self.err, stream)
+
+    def run_fill(self, stream=None) -> None:
+        if self.fill is not None:
+            self.append(self.fill, stream)
+
+    def run_step(self, i: int, stream=None, layers: Optional[int] = None) -> None:
+        """append -> select -> every cross-decoder layer, all enqueued on one stream."""
+        ds = self.steps[i]
+        self.append(ds, stream)
+        self.select(ds, stream)
+        for layer in range(self.wl.layers if layers is None else layers):
+            self.attend(ds, layer, stream)
+
+    def run_all(self, stream=None) -> None:
+        self.run_fill(stream)
+        for i in range(len(self.steps)):
+            self.run_step(i, stream)
+
+    def error_bits(self) -> int:
+        return int(self.err.item())
