@@ -79,10 +79,15 @@ def test_host_validation_rejects_before_launch(lib_path):
     assert L.yoco_select_cross_rows(None, None, 3, None, None, None, None, None) == 1
 
 
-def test_workspace_size_grows_with_context(lib_path):
+def test_workspace_sizes(lib_path):
     from yoco_shared_kv_gb300 import _native as N
     import torch
-    small = N.yoco_cross_attn_workspace_size(4, 16, 1, 128, 32, 4096, torch.bfloat16)
-    big = N.yoco_cross_attn_workspace_size(4, 16, 1, 128, 32, 131072, torch.bfloat16)
+    # fp32 split-KV path: partials grow with the longest context
+    small = N.yoco_cross_attn_workspace_size(4, 16, 1, 128, 32, 4096, torch.float32)
+    big = N.yoco_cross_attn_workspace_size(4, 16, 1, 128, 32, 131072, torch.float32)
     assert big > small >= 0
+    # bf16 persistent path: two partials per worker, independent of context length
+    a = N.yoco_cross_attn_workspace_size(4, 16, 1, 128, 32, 4096, torch.bfloat16)
+    b = N.yoco_cross_attn_workspace_size(64, 16, 1, 128, 32, 131072, torch.bfloat16)
+    assert a == b > 0
     assert N.yoco_cross_attn_workspace_size(4, 16, 1, 96, 32, 4096, torch.bfloat16) == 0

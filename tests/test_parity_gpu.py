@@ -180,10 +180,36 @@ def test_attention_single_key_and_block_edges(P):
 
 
 @pytest.mark.parametrize("H_q,H_kv,D,bs", [(4, 4, 64, 16), (6, 2, 128, 32), (12, 1, 64, 32),
-                                           (16, 2, 256, 16), (2, 1, 128, 16), (16, 16, 128, 32)])
+                                           (16, 2, 256, 16), (2, 1, 128, 16), (16, 16, 128, 32),
+                                           (16, 1, 256, 32), (32, 2, 256, 16), (8, 1, 64, 16)])
 def test_attention_shapes(P, H_q, H_kv, D, bs):
     wl = pure_decode(4000 + H_q * 7 + D, num_reqs=5, ctx_lo=1, ctx_hi=900, H_q=H_q, H_kv=H_kv,
                      D=D, bs=bs, layers=2)
+    dw = P.DeviceWorkload(wl)
+    dw.run_all()
+    torch.cuda.synchronize()
+    assert dw.error_bits() == 0
+    got = gpu_out(dw.steps[0].out)
+    ref = oracle_step_out(wl, wl.steps[0])
+    assert np.abs(got - ref).max() <= ATOL["bf16"]
+
+
+def test_attention_fewer_pages_than_workers(P):
+    """A batch of a few short rows: most CTAs and warps of the persistent grid get no page."""
+    for lens in ([5], [1, 3], [40, 1, 17]):
+        wl = pure_decode(3100 + len(lens), explicit_lens=lens, layers=2)
+        dw = P.DeviceWorkload(wl)
+        dw.run_all()
+        torch.cuda.synchronize()
+        assert dw.error_bits() == 0
+        got = gpu_out(dw.steps[0].out)
+        ref = oracle_step_out(wl, wl.steps[0])
+        assert np.abs(got - ref).max() <= ATOL["bf16"], lens
+
+
+def test_attention_one_long_row_many_ctas(P):
+    """One row far longer than a CTA slice: its pieces are merged across many CTAs."""
+    wl = pure_decode(3200, explicit_lens=[60000], H_q=16, H_kv=1, D=128, bs=32, layers=2)
     dw = P.DeviceWorkload(wl)
     dw.run_all()
     torch.cuda.synchronize()

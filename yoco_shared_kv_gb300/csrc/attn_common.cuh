@@ -1,0 +1,55 @@
+// Shared definitions of the cross-decoder attention kernels (internal).
+#pragma once
+
+#include "common.cuh"
+
+namespace yoco {
+
+// Launch parameters common to both attention paths.
+struct AttnParams {
+    const void* q;              // [max_rows][H_q][D]
+    void* out;                  // [max_rows][H_q][D]
+    const int32_t* block_table; // [num_reqs][max_blocks]
+    const int32_t* seq_lens;    // [num_reqs]
+    const int32_t* cqsl;        // [num_reqs + 1] cross query_start_loc
+    float* ws_o;                // partial outputs (layout depends on the path)
+    float2* ws_ml;              // partial (running max in log2 units, sum)
+    int32_t* err;
+    int32_t max_blocks;
+    int32_t num_reqs;
+    int32_t max_rows;
+    int32_t H_q, H_kv, G;
+    int32_t num_blocks;
+    int32_t block_size;
+    int32_t split_pages;        // CUDA-core path: logical pages per split
+    int32_t max_splits;         // CUDA-core path
+    float scale_log2;           // softmax scale * log2(e)
+};
+
+// Wait limit for one asynchronous page copy before a kernel gives up.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+__device__ __forceinline__ bool launch_aborted(const AttnParams& p) {
+    return p.err != nullptr &&
+           (*reinterpret_cast<volatile int32_t*>(p.err) & YOCO_DEVERR_TIMEOUT) != 0;
+}
+
+template <typename T>
+__device__ __forceinline__ T from_float(float x);
+template <>
+__device__ __forceinline__ float from_float<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+// Host-side launchers (one per path). `tc_workspace_bytes` / `cc_*` give the
+// scratch each path needs.
+size_t tc_workspace_bytes(int sms, int H_kv, int G, int D, int BS);
+int tc_ctas(int sms);
+cudaError_t launch_attn_tc(const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p,
+                           int D, int BS, int sms, cudaStream_t s);
+cudaError_t launch_attn_cc(const void* k_cache, const void* v_cache, const AttnParams& p, int D,
+                           int hb, cudaStream_t s);
+
+}  // namespace yoco

@@ -1,0 +1,696 @@
+// Tensor-core (bf16) cross-decoder attention: persistent and page-balanced.
+//
+// "KV cache memory systems", "Cache contents": out = softmax(q K^T/sqrt(d_h)) V
+// over the cached keys; "Contiguous allocation wastes capacity": every
+// logical block is resolved through the block table. "YOCO 论文与推理数据流
+// 详解" §10.4/§11: each cross-decoder layer streams the whole shared cache
+// once with its own queries, so a layer is an HBM stream.
+//
+// Work decomposition. The unit of work is a page of one (cross row, kv head)
+// segment. Segments are laid out in the order (row, kv head) and their pages
+// form one flattened sequence of P pages. The grid has one CTA per SM; CTA c
+// owns pages [P c / C, P (c+1) / C) and each of its NW warps owns an equal
+// contiguous slice of that, streamed through the warp's own TMA ring. Every
+// worker therefore moves the same number of bytes, whatever the length mix,
+// and the ring never drains between segments.
+//   - A segment that lies inside one warp's slice is finished in registers
+//     and written straight to `out`.
+//   - A segment cut by a warp boundary leaves a partial (m, l, o) per piece;
+//     at the end of the kernel the CTA combines the pieces of each segment
+//     it holds, writing `out` when the CTA holds the whole segment and a
+//     CTA-level partial otherwise.
+//   - A segment cut by a CTA boundary is finished by attn_tc_merge, which
+//     combines the CTA partials in CTA order.
+// Every combine runs in a fixed order that depends only on logical page
+// indices, so the output is bit-identical under any physical page placement.
+//
+// Per page (one kv head, block_size tokens): K and V arrive by TMA as
+// head_dim/64 tiles of [block_size x 128 B] with the 128-byte swizzle (so
+// ldmatrix is conflict free); S^T = K Q^T and O^T += V^T P^T are m16n8k16
+// bf16 mma.sync products with fp32 accumulators, the group's query heads on
+// the N side; P moves from the accumulator layout to the B-operand layout
+// with movmatrix. The online softmax works in the log2 domain.
+#include "attn_common.cuh"
+
+namespace yoco {
+namespace {
+
+template <int D, int BS>
+struct TcShape {
+    static constexpr int PAGE_BYTES = BS * D * 2;       // K (or V) of one page, one kv head
+    static constexpr int STAGE_BYTES = 2 * PAGE_BYTES;  // K + V
+    static constexpr int NW = STAGE_BYTES <= 8192 ? 8 : (STAGE_BYTES <= 16384 ? 4 : 2);
+    static constexpr int STAGES = 3;
+    static constexpr int KSUB = D / 64;  // 128-byte swizzled sub-tiles per row
+    static constexpr int SUB_BYTES = BS * 128;
+    static constexpr int MT = BS / 16;   // 16-token tiles per page
+    static constexpr int KD = D / 16;    // 16-wide steps along head_dim
+    static constexpr int SMEM = NW * STAGES * STAGE_BYTES + 1024;
+};
+
+// Byte offset of (token t, 16-byte chunk j of head-dim sub-tile c) in a
+// 128B-swizzled page tile.
+template <int BS>
+__device__ __forceinline__ uint32_t swz(int c, int t, int j) {
+    return static_cast<uint32_t>(c * (BS * 128) + t * 128 + ((j ^ (t & 7)) << 4));
+}
+
+// ------------------------------------------------------------- work order
+
+__device__ __forceinline__ int32_t row_pages(int32_t kv_len, int32_t cap, int32_t bs) {
+    if (kv_len <= 0) return 0;
+    if (kv_len > cap) kv_len = cap;
+    return (kv_len + bs - 1) / bs;
+}
+
+// Pages (all kv heads) of request r's cross rows below max_rows.
+__device__ __forceinline__ int64_t req_pages(const AttnParams& p, int32_t r, int32_t cap) {
+    const int32_t c0 = __ldg(p.cqsl + r), c1 = __ldg(p.cqsl + r + 1);
+    const int32_t k = c1 - c0, hi = min(c1, p.max_rows), seq = __ldg(p.seq_lens + r);
+    int64_t s = 0;
+    for (int32_t n = c0; n < hi; ++n) s += row_pages(seq - k + (n - c0) + 1, cap, p.block_size);
+    return s * p.H_kv;
+}
+
+__device__ __forceinline__ int64_t warp_sum64(int64_t v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
+__device__ __forceinline__ int64_t warp_incl_scan64(int64_t v, int lane) {
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int64_t t = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += t;
+    }
+    return v;
+}
+
+// Total pages of the launch (every lane of the warp returns it).
+__device__ int64_t total_pages(const AttnParams& p, int lane, int32_t cap) {
+    int64_t tot = 0;
+    for (int32_t base = 0; base < p.num_reqs; base += 32) {
+        const int32_t r = base + lane;
+        tot += warp_sum64(r < p.num_reqs ? req_pages(p, r, cap) : 0);
+    }
+    return tot;
+}
+
+// Position in the flattened (row, kv head, page) sequence.
+struct Cursor {
+    int64_t seg_start;  // flattened index of the segment's first page
+    int32_t req, n, g, pp, kv_len, pages;
+};
+
+// Cursor of flattened page x (< total). Warp-collective; all lanes agree.
+__device__ void locate(const AttnParams& p, int lane, int64_t x, int32_t cap, Cursor& c) {
+    int64_t done = 0;
+    c.req = -1;
+    for (int32_t base = 0; base < p.num_reqs; base += 32) {
+        const int32_t r = base + lane;
+        const int64_t v = r < p.num_reqs ? req_pages(p, r, cap) : 0;
+        const int64_t incl = warp_incl_scan64(v, lane);
+        const int64_t chunk = __shfl_sync(0xffffffffu, incl, 31);
+        if (done + chunk > x) {
+            const unsigned m = __ballot_sync(0xffffffffu, done + incl > x);
+            const int src = __ffs(m) - 1;
+            int64_t off = done + __shfl_sync(0xffffffffu, incl - v, src);
+            const int32_t req = base + src;
+            const int32_t c0 = __ldg(p.cqsl + req), c1 = __ldg(p.cqsl + req + 1);
+            const int32_t k = c1 - c0, seq = __ldg(p.seq_lens + req);
+            for (int32_t n = c0; n < c1 && n < p.max_rows; ++n) {
+                const int32_t kv = seq - k + (n - c0) + 1;
+                const int32_t pg = row_pages(kv, cap, p.block_size);
+                const int64_t seg_pages = static_cast<int64_t>(pg) * p.H_kv;
+                if (x < off + seg_pages) {
+                    const int64_t rel = x - off;
+                    c.req = req;
+                    c.n = n;
+                    c.kv_len = min(kv, cap);
+                    c.pages = pg;
+                    c.g = static_cast<int32_t>(rel / pg);
+                    c.pp = static_cast<int32_t>(rel - static_cast<int64_t>(c.g) * pg);
+                    c.seg_start = off + static_cast<int64_t>(c.g) * pg;
+                    return;
+                }
+                off += seg_pages;
+            }
+            return;
+        }
+        done += chunk;
+    }
+}
+
+// Next page in the flattened order (skips rows without keys).
+__device__ __forceinline__ void advance(const AttnParams& p, Cursor& c, int32_t cap) {
+    if (++c.pp < c.pages) return;
+    c.seg_start += c.pages;
+    c.pp = 0;
+    if (++c.g < p.H_kv) return;
+    c.g = 0;
+    for (;;) {
+        if (++c.n >= p.max_rows) return;
+        while (c.req + 1 < p.num_reqs && __ldg(p.cqsl + c.req + 1) <= c.n) ++c.req;
+        const int32_t c0 = __ldg(p.cqsl + c.req), c1 = __ldg(p.cqsl + c.req + 1);
+        if (c.n >= c1) return;
+        const int32_t kv = __ldg(p.seq_lens + c.req) - (c1 - c0) + (c.n - c0) + 1;
+        c.pages = row_pages(kv, cap, p.block_size);
+        c.kv_len = min(kv, cap);
+        if (c.pages > 0) return;
+    }
+}
+
+// Index of the worker (of `workers` equal slices of P) owning flattened page x.
+__device__ __forceinline__ int32_t owner(int64_t x, int64_t P, int32_t workers) {
+    return static_cast<int32_t>(((x + 1) * workers - 1) / P);
+}
+
+struct PieceHdr {
+    int64_t s0, s1;  // segment [first page, end) in the flattened order
+    int32_t n, g;
+    int32_t valid;
+};
+
+// Workspace carve-up (floats): warp pieces then CTA pieces, outputs then stats.
+struct TcWs {
+    float* w_o;
+    float* c_o;
+    float2* w_ml;
+    float2* c_ml;
+};
+
+__device__ __forceinline__ TcWs tc_ws(const AttnParams& p, int ctas, int nw, int D) {
+    TcWs w;
+    const int64_t per = 2ll * p.G;  // pieces per worker (first / last segment) x heads
+    const int64_t W = static_cast<int64_t>(ctas) * nw;
+    w.w_o = p.ws_o;
+    w.c_o = p.ws_o + W * per * D;
+    w.w_ml = p.ws_ml;
+    w.c_ml = p.ws_ml + W * per;
+    return w;
+}
+
+// --------------------------------------------------------------- kernel
+
+template <int D, int BS, int NT>
+__global__ void __launch_bounds__(TcShape<D, BS>::NW * 32, 1)
+    attn_tc_persistent(const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
+    using S = TcShape<D, BS>;
+    constexpr int NW = S::NW, STAGES = S::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bars[NW * STAGES];
+    __shared__ PieceHdr hdr[NW][2];
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gl = lane >> 2, tq = lane & 3;  // mma fragment row group / column pair
+    if (threadIdx.x == 0) abort_flag = launch_aborted(p) ? 1 : 0;
+    if (lane == 0) {
+        for (int i = 0; i < STAGES; ++i) mbar_init(&bars[warp * STAGES + i], 1);
+        fence_mbar_init();
+        hdr[warp][0].valid = hdr[warp][1].valid = 0;
+    }
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+    }
+    __syncthreads();
+    if (abort_flag) return;
+
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    const int64_t cap64 = static_cast<int64_t>(p.max_blocks) * BS;
+    const int32_t cap = cap64 > 0x7fffffff ? 0x7fffffff : static_cast<int32_t>(cap64);
+    const int64_t P = total_pages(p, lane, cap);
+    const int64_t C = gridDim.x;
+    const int64_t cta_lo = P * blockIdx.x / C, cta_hi = P * (blockIdx.x + 1) / C;
+    const int64_t my_lo = cta_lo + (cta_hi - cta_lo) * warp / NW;
+    const int64_t my_hi = cta_lo + (cta_hi - cta_lo) * (warp + 1) / NW;
+    const int32_t n_my = static_cast<int32_t>(my_hi - my_lo);
+    const int32_t wid = blockIdx.x * NW + warp;
+    const TcWs ws = tc_ws(p, gridDim.x, NW, D);
+
+    uint8_t* wbuf = smem + warp * STAGES * S::STAGE_BYTES;
+    uint64_t* wbar = bars + warp * STAGES;
+    Cursor cc;  // page being consumed
+    cc.req = -1;
+    if (n_my > 0) locate(p, lane, my_lo, cap, cc);
+    Cursor pc = cc;  // next page to issue (lane 0)
+
+    auto issue = [&](int i) {  // lane 0 only; pc is at page i
+        const int st = i % STAGES;
+        uint64_t* bar = wbar + st;
+        const int32_t blk = __ldg(p.block_table + static_cast<int64_t>(pc.req) * p.max_blocks + pc.pp);
+        if (blk < 0 || blk >= p.num_blocks) {
+            set_err(p.err, YOCO_DEVERR_PAGE_RANGE);
+            mbar_arrive(bar);
+        } else {
+            mbar_arrive_expect_tx(bar, 2 * S::PAGE_BYTES);
+            uint8_t* kd = wbuf + st * S::STAGE_BYTES;
+            uint8_t* vd = kd + S::PAGE_BYTES;
+            const int32_t y = (blk * p.H_kv + pc.g) * BS;
+#pragma unroll
+            for (int c = 0; c < S::KSUB; ++c) {
+                tma_load_2d(kd + c * S::SUB_BYTES, &tm_k, c * 64, y, bar);
+                tma_load_2d(vd + c * S::SUB_BYTES, &tm_v, c * 64, y, bar);
+            }
+        }
+        advance(p, pc, cap);
+    };
+    if (lane == 0) {
+        const int pro = n_my < STAGES ? n_my : STAGES;
+        for (int i = 0; i < pro; ++i) issue(i);
+    }
+
+    uint32_t qf[S::KD][NT][2];
+    float o[S::KD][NT][4];
+    float m_run[NT][2], l_part[NT][2];
+    auto reset_state = [&]() {
+#pragma unroll
+        for (int a = 0; a < S::KD; ++a)
+#pragma unroll
+            for (int b = 0; b < NT; ++b)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) o[a][b][c] = 0.f;
+#pragma unroll
+        for (int b = 0; b < NT; ++b) {
+            m_run[b][0] = m_run[b][1] = -INFINITY;
+            l_part[b][0] = l_part[b][1] = 0.f;
+        }
+    };
+    // B operand of S^T = K Q^T: head gl of n-tile nt, head dims 2tq.. of each 16-wide step
+    auto load_q = [&](int32_t n, int32_t g) {
+        const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(p.q) +
+                                    (static_cast<int64_t>(n) * p.H_q + g * p.G) * D;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int h = nt * 8 + gl;
+            const bool ok = h < p.G;
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(qrow + (ok ? h : 0) * D);
+#pragma unroll
+            for (int kk = 0; kk < S::KD; ++kk) {
+                qf[kk][nt][0] = ok ? __ldg(src + kk * 8 + tq) : 0u;
+                qf[kk][nt][1] = ok ? __ldg(src + kk * 8 + 4 + tq) : 0u;
+            }
+        }
+    };
+    reset_state();
+    const float sl2 = p.scale_log2;
+    bool aborted = false;
+    int consumed = 0;
+
+    for (int i = 0; i < n_my; ++i) {
+        if (i == 0 || cc.pp == 0) load_q(cc.n, cc.g);
+        const int st = i % STAGES;
+        if (!mbar_wait_bounded(wbar + st, (i / STAGES) & 1, kWaitLimitNs)) {
+            aborted = true;
+            break;
+        }
+        consumed = i + 1;
+        const int32_t blk = __ldg(p.block_table + static_cast<int64_t>(cc.req) * p.max_blocks + cc.pp);
+        if (blk >= 0 && blk < p.num_blocks) {
+            const uint32_t kbase = smem_u32(wbuf + st * S::STAGE_BYTES);
+            const uint32_t vbase = kbase + S::PAGE_BYTES;
+            const int32_t nvalid = min(BS, cc.kv_len - cc.pp * BS);
+            if (nvalid < BS) {
+                // Rows past the causal end may hold stale data (even NaN), and a
+                // zero probability times NaN is NaN: clear those V rows first.
+                uint8_t* vd = wbuf + st * S::STAGE_BYTES + S::PAGE_BYTES;
+                const int nbytes = (BS - nvalid) * 128;
+                for (int c = 0; c < S::KSUB; ++c)
+                    for (int b = lane * 16; b < nbytes; b += 32 * 16)
+                        *reinterpret_cast<uint4*>(vd + c * S::SUB_BYTES + nvalid * 128 + b) =
+                            make_uint4(0, 0, 0, 0);
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            // ---- S^T = K Q^T (tokens x heads); two accumulators halve the chain ----
+            float sc[S::MT][NT][4];
+            {
+                float sc2[S::MT][NT][4];
+#pragma unroll
+                for (int mt = 0; mt < S::MT; ++mt)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) sc[mt][nt][c] = sc2[mt][nt][c] = 0.f;
+                const int mi = lane >> 3, rr = lane & 7;
+#pragma unroll
+                for (int mt = 0; mt < S::MT; ++mt) {
+                    const int t = mt * 16 + (mi & 1) * 8 + rr;
+#pragma unroll
+                    for (int kk = 0; kk < S::KD; ++kk) {
+                        uint32_t a0, a1, a2, a3;
+                        ldsm_x4(kbase + swz<BS>(kk >> 2, t, (kk & 3) * 2 + (mi >> 1)), a0, a1,
+                                a2, a3);
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            if (kk & 1)
+                                mma_bf16_16816(sc2[mt][nt], a0, a1, a2, a3, qf[kk][nt][0],
+                                               qf[kk][nt][1]);
+                            else
+                                mma_bf16_16816(sc[mt][nt], a0, a1, a2, a3, qf[kk][nt][0],
+                                               qf[kk][nt][1]);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int mt = 0; mt < S::MT; ++mt)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) sc[mt][nt][c] += sc2[mt][nt][c];
+            }
+            // ---- online softmax ----
+            float corr[NT][2];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+                for (int mt = 0; mt < S::MT; ++mt) {
+                    const int t0 = mt * 16 + gl, t1 = t0 + 8;
+                    float* c = sc[mt][nt];
+                    c[0] = t0 < nvalid ? c[0] * sl2 : -INFINITY;
+                    c[1] = t0 < nvalid ? c[1] * sl2 : -INFINITY;
+                    c[2] = t1 < nvalid ? c[2] * sl2 : -INFINITY;
+                    c[3] = t1 < nvalid ? c[3] * sl2 : -INFINITY;
+                    mx0 = fmaxf(mx0, fmaxf(c[0], c[2]));
+                    mx1 = fmaxf(mx1, fmaxf(c[1], c[3]));
+                }
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                }
+                const float mn0 = fmaxf(m_run[nt][0], mx0), mn1 = fmaxf(m_run[nt][1], mx1);
+                corr[nt][0] = exp2_approx(m_run[nt][0] - mn0);
+                corr[nt][1] = exp2_approx(m_run[nt][1] - mn1);
+                m_run[nt][0] = mn0;
+                m_run[nt][1] = mn1;
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                if (corr[nt][0] != 1.f || corr[nt][1] != 1.f) {
+#pragma unroll
+                    for (int md = 0; md < S::KD; ++md) {
+                        o[md][nt][0] *= corr[nt][0];
+                        o[md][nt][1] *= corr[nt][1];
+                        o[md][nt][2] *= corr[nt][0];
+                        o[md][nt][3] *= corr[nt][1];
+                    }
+                }
+                l_part[nt][0] *= corr[nt][0];
+                l_part[nt][1] *= corr[nt][1];
+            }
+            // ---- O^T += V^T P^T ----
+#pragma unroll
+            for (int kt = 0; kt < S::MT; ++kt) {
+                uint32_t pb[NT][2];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const float* c = sc[kt][nt];
+                    const uint32_t lo = pack_bf16x2(exp2_approx(c[0] - m_run[nt][0]),
+                                                    exp2_approx(c[1] - m_run[nt][1]));
+                    const uint32_t hi = pack_bf16x2(exp2_approx(c[2] - m_run[nt][0]),
+                                                    exp2_approx(c[3] - m_run[nt][1]));
+                    // row sums use exactly the rounded weights fed to the mma
+                    l_part[nt][0] += bf16lo_to_f32(lo) + bf16lo_to_f32(hi);
+                    l_part[nt][1] += bf16hi_to_f32(lo) + bf16hi_to_f32(hi);
+                    pb[nt][0] = movmatrix_trans(lo);
+                    pb[nt][1] = movmatrix_trans(hi);
+                }
+                const int mi = lane >> 3, rr = lane & 7;
+                const int t = kt * 16 + (mi >> 1) * 8 + rr;
+#pragma unroll
+                for (int md = 0; md < S::KD; ++md) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4_trans(vbase + swz<BS>(md >> 2, t, (md & 3) * 2 + (mi & 1)), a0, a1,
+                                  a2, a3);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        mma_bf16_16816(o[md][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0 && i + STAGES < n_my) issue(i + STAGES);
+
+        if (cc.pp == cc.pages - 1 || i == n_my - 1) {  // segment (or slice) ends here
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    l_part[nt][0] += __shfl_xor_sync(0xffffffffu, l_part[nt][0], off);
+                    l_part[nt][1] += __shfl_xor_sync(0xffffffffu, l_part[nt][1], off);
+                }
+            const int64_t s0 = cc.seg_start, s1 = cc.seg_start + cc.pages;
+            const int64_t head0 = static_cast<int64_t>(cc.n) * p.H_q + cc.g * p.G;
+            if (s0 >= my_lo && s1 <= my_hi) {
+                // whole segment in this warp: final output
+                __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int h = nt * 8 + 2 * tq + e;
+                        if (h >= p.G) continue;
+                        const float inv = 1.f / l_part[nt][e];
+                        __nv_bfloat16* dst = outp + (head0 + h) * D;
+#pragma unroll
+                        for (int md = 0; md < S::KD; ++md) {
+                            dst[md * 16 + gl] = __float2bfloat16_rn(o[md][nt][e] * inv);
+                            dst[md * 16 + gl + 8] = __float2bfloat16_rn(o[md][nt][2 + e] * inv);
+                        }
+                    }
+            } else {
+                const int slot = s0 < my_lo ? 0 : 1;
+                const int64_t piece = (static_cast<int64_t>(wid) * 2 + slot) * p.G;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int h = nt * 8 + 2 * tq + e;
+                        if (h >= p.G) continue;
+                        float* dst = ws.w_o + (piece + h) * D;
+#pragma unroll
+                        for (int md = 0; md < S::KD; ++md) {
+                            dst[md * 16 + gl] = o[md][nt][e];
+                            dst[md * 16 + gl + 8] = o[md][nt][2 + e];
+                        }
+                        if (gl == 0) ws.w_ml[piece + h] = make_float2(m_run[nt][e], l_part[nt][e]);
+                    }
+                if (lane == 0) {
+                    hdr[warp][slot].s0 = s0;
+                    hdr[warp][slot].s1 = s1;
+                    hdr[warp][slot].n = cc.n;
+                    hdr[warp][slot].g = cc.g;
+                    hdr[warp][slot].valid = 1;
+                }
+            }
+            reset_state();
+        }
+        advance(p, cc, cap);
+    }
+
+    if (aborted) {
+        // drain this warp's copies still in flight before the CTA exits
+        const int issued = n_my < consumed + STAGES ? n_my : consumed + STAGES;
+        for (int i = consumed; i < issued; ++i)
+            (void)mbar_wait_bounded(wbar + (i % STAGES), (i / STAGES) & 1, kWaitLimitNs);
+        if (lane == 0) {
+            set_err(p.err, YOCO_DEVERR_TIMEOUT);
+            atomicExch(&abort_flag, 1);
+        }
+    }
+    __syncthreads();  // warp pieces are in global memory, headers in shared memory
+    if (abort_flag) return;
+
+    // ---- combine the pieces of each segment this CTA holds, in warp order ----
+    __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out);
+    int e0 = 0;  // index into the flattened (warp, slot) header list
+    while (e0 < 2 * NW) {
+        if (!hdr[e0 >> 1][e0 & 1].valid) {
+            ++e0;
+            continue;
+        }
+        const PieceHdr H = hdr[e0 >> 1][e0 & 1];
+        int e1 = e0 + 1;  // group = following headers up to the next other segment
+        while (e1 < 2 * NW) {
+            const PieceHdr& X = hdr[e1 >> 1][e1 & 1];
+            if (X.valid && X.s0 != H.s0) break;
+            ++e1;
+        }
+        const bool whole = H.s0 >= cta_lo && H.s1 <= cta_hi;
+        const int cslot = H.s0 < cta_lo ? 0 : 1;
+        const int64_t head0 = static_cast<int64_t>(H.n) * p.H_q + H.g * p.G;
+        for (int idx = threadIdx.x; idx < p.G * D; idx += blockDim.x) {
+            const int h = idx / D, d = idx - (idx / D) * D;
+            float M = -INFINITY;
+            for (int e = e0; e < e1; ++e) {
+                if (!hdr[e >> 1][e & 1].valid) continue;
+                const int64_t pc_ = (static_cast<int64_t>(blockIdx.x * NW + (e >> 1)) * 2 + (e & 1)) * p.G;
+                M = fmaxf(M, ws.w_ml[pc_ + h].x);
+            }
+            float L = 0.f, O = 0.f;
+            for (int e = e0; e < e1; ++e) {
+                if (!hdr[e >> 1][e & 1].valid) continue;
+                const int64_t pc_ = (static_cast<int64_t>(blockIdx.x * NW + (e >> 1)) * 2 + (e & 1)) * p.G;
+                const float2 ml = ws.w_ml[pc_ + h];
+                if (ml.x == -INFINITY) continue;
+                const float f = exp2_approx(ml.x - M);
+                L += ml.y * f;
+                O += ws.w_o[(pc_ + h) * D + d] * f;
+            }
+            if (whole) {
+                outp[(head0 + h) * D + d] = __float2bfloat16_rn(O / L);
+            } else {
+                const int64_t cp = (static_cast<int64_t>(blockIdx.x) * 2 + cslot) * p.G + h;
+                ws.c_o[cp * D + d] = O;
+                if (d == 0) ws.c_ml[cp] = make_float2(M, L);
+            }
+        }
+        e0 = e1;
+    }
+}
+
+// Combines the CTA-level partials of every segment cut by a CTA boundary
+// (grid: one CTA per split-kernel CTA x query head of a group; D threads),
+// and zero-fills rows that have no key. Runs after attn_tc_persistent.
+template <int D, int NW>
+__global__ void __launch_bounds__(D) attn_tc_merge(const AttnParams p, int32_t ctas) {
+    __shared__ float sM, sL;
+    const int32_t c = blockIdx.x, h = blockIdx.y;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t cap64 = static_cast<int64_t>(p.max_blocks) * p.block_size;
+    const int32_t cap = cap64 > 0x7fffffff ? 0x7fffffff : static_cast<int32_t>(cap64);
+    __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out);
+
+    // rows with no key to attend: zero output, flag (rows spread over the CTAs)
+    if (h == 0 && p.num_reqs > 0) {
+        const int32_t rows = min(__ldg(p.cqsl + p.num_reqs), p.max_rows);
+        for (int32_t n = c; n < rows; n += ctas) {
+            int32_t req, kv;
+            if (!locate_row(p.cqsl, p.num_reqs, n, p.seq_lens, req, kv)) break;
+            if (kv <= 0) {
+                for (int i = threadIdx.x; i < p.H_q * D; i += blockDim.x)
+                    outp[static_cast<int64_t>(n) * p.H_q * D + i] = __float2bfloat16_rn(0.f);
+                if (threadIdx.x == 0) set_err(p.err, YOCO_DEVERR_EMPTY_ROW);
+            } else if (kv > cap && threadIdx.x == 0) {
+                set_err(p.err, YOCO_DEVERR_POS_RANGE);
+            }
+        }
+    }
+    if (launch_aborted(p)) return;
+    if (c == 0) return;  // CTA 0's start is never strictly inside a segment
+
+    // the segment holding this CTA's first page (all warps compute it)
+    const int64_t P = total_pages(p, lane, cap);
+    const int64_t lo = P * c / ctas;
+    if (lo >= P) return;
+    Cursor cur;
+    locate(p, lane, lo, cap, cur);
+    if (cur.req < 0) return;
+    const int64_t s0 = cur.seg_start, s1 = cur.seg_start + cur.pages;
+    const int32_t c_first = owner(s0, P, ctas);
+    if (c != c_first + 1) return;  // only the first CTA starting inside the segment merges
+    const int32_t c_last = owner(s1 - 1, P, ctas);
+    const TcWs ws = tc_ws(p, ctas, NW, D);
+    // A CTA keeps slot 0 for a segment that began before its slice and slot 1
+    // for one that begins inside it; only c_first holds the segment's start.
+    auto piece_of = [&](int32_t cc_) -> int64_t {
+        const int slot = cc_ == c_first ? 1 : 0;
+        return (static_cast<int64_t>(cc_) * 2 + slot) * p.G + h;
+    };
+    auto nonempty = [&](int32_t cc_) { return P * cc_ / ctas < P * (cc_ + 1) / ctas; };
+    if (warp == 0) {
+        float M = -INFINITY;
+        for (int32_t cc_ = c_first + lane; cc_ <= c_last; cc_ += 32)
+            if (nonempty(cc_)) M = fmaxf(M, ws.c_ml[piece_of(cc_)].x);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        float L = 0.f;
+        for (int32_t cc_ = c_first + lane; cc_ <= c_last; cc_ += 32)
+            if (nonempty(cc_)) {
+                const float2 ml = ws.c_ml[piece_of(cc_)];
+                if (ml.x != -INFINITY) L += ml.y * exp2_approx(ml.x - M);
+            }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+        if (lane == 0) {
+            sM = M;
+            sL = L;
+        }
+    }
+    __syncthreads();
+    const float M = sM, invL = 1.f / sL;
+    const int d = threadIdx.x;
+    float acc = 0.f;
+    for (int32_t cc_ = c_first; cc_ <= c_last; ++cc_) {
+        if (!nonempty(cc_)) continue;
+        const int64_t pc_ = piece_of(cc_);
+        const float2 ml = ws.c_ml[pc_];
+        if (ml.x == -INFINITY) continue;
+        acc += ws.c_o[pc_ * D + d] * exp2_approx(ml.x - M);
+    }
+    const int64_t head = static_cast<int64_t>(cur.n) * p.H_q + cur.g * p.G + h;
+    outp[head * D + d] = __float2bfloat16_rn(acc * invL);
+}
+
+template <int D, int BS, int NT>
+cudaError_t launch_one(const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p, int sms,
+                       cudaStream_t s) {
+    using S = TcShape<D, BS>;
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_persistent<D, BS, NT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+    if (e != cudaSuccess) return e;
+    const int ctas = tc_ctas(sms);
+    attn_tc_persistent<D, BS, NT><<<ctas, S::NW * 32, S::SMEM, s>>>(mk, mv, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    attn_tc_merge<D, S::NW><<<dim3(ctas, p.G), D, 0, s>>>(p, ctas);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p, int BS,
+                     int sms, cudaStream_t s) {
+    const bool wide = p.G > 8;
+    if (BS == 16) return wide ? launch_one<D, 16, 2>(mk, mv, p, sms, s)
+                              : launch_one<D, 16, 1>(mk, mv, p, sms, s);
+    return wide ? launch_one<D, 32, 2>(mk, mv, p, sms, s) : launch_one<D, 32, 1>(mk, mv, p, sms, s);
+}
+
+int tc_nw(int D, int BS) {
+    switch (D * 100 + BS) {
+        case 6416: return TcShape<64, 16>::NW;
+        case 6432: return TcShape<64, 32>::NW;
+        case 12816: return TcShape<128, 16>::NW;
+        case 12832: return TcShape<128, 32>::NW;
+        case 25616: return TcShape<256, 16>::NW;
+        default: return TcShape<256, 32>::NW;
+    }
+}
+
+}  // namespace
+
+int tc_ctas(int sms) { return sms; }
+
+size_t tc_workspace_bytes(int sms, int H_kv, int G, int D, int BS) {
+    (void)H_kv;
+    const size_t ctas = static_cast<size_t>(tc_ctas(sms));
+    const size_t W = ctas * tc_nw(D, BS);
+    return (W + ctas) * 2 * static_cast<size_t>(G) * (static_cast<size_t>(D) * 4 + 8);
+}
+
+cudaError_t launch_attn_tc(const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p,
+                           int D, int BS, int sms, cudaStream_t s) {
+    switch (D) {
+        case 64: return launch_d<64>(mk, mv, p, BS, sms, s);
+        case 128: return launch_d<128>(mk, mv, p, BS, sms, s);
+        default: return launch_d<256>(mk, mv, p, BS, sms, s);
+    }
+}
+
+}  // namespace yoco
