@@ -35,12 +35,22 @@
 namespace yoco {
 namespace {
 
+// Warps per CTA and ring depth per warp for 16 KiB stages (compile-time
+// tunables; the defaults fill about 192 KiB of shared memory).
+#ifndef YOCO_TC_NW16
+#define YOCO_TC_NW16 4
+#endif
+#ifndef YOCO_TC_ST16
+#define YOCO_TC_ST16 3
+#endif
+
 template <int D, int BS>
 struct TcShape {
     static constexpr int PAGE_BYTES = BS * D * 2;       // K (or V) of one page, one kv head
     static constexpr int STAGE_BYTES = 2 * PAGE_BYTES;  // K + V
-    static constexpr int NW = STAGE_BYTES <= 8192 ? 8 : (STAGE_BYTES <= 16384 ? 4 : 2);
-    static constexpr int STAGES = 3;
+    static constexpr int NW =
+        STAGE_BYTES <= 8192 ? 8 : (STAGE_BYTES <= 16384 ? YOCO_TC_NW16 : 2);
+    static constexpr int STAGES = STAGE_BYTES == 16384 ? YOCO_TC_ST16 : 3;
     static constexpr int KSUB = D / 64;  // 128-byte swizzled sub-tiles per row
     static constexpr int SUB_BYTES = BS * 128;
     static constexpr int MT = BS / 16;   // 16-token tiles per page
@@ -201,6 +211,7 @@ __global__ void __launch_bounds__(TcShape<D, BS>::NW * 32, 1)
     constexpr int NW = S::NW, STAGES = S::STAGES;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bars[NW * STAGES];
+    __shared__ int32_t stage_blk[NW * STAGES];  // physical page of each stage (-1: invalid)
     __shared__ PieceHdr hdr[NW][2];
     __shared__ int abort_flag;
 
@@ -243,6 +254,8 @@ __global__ void __launch_bounds__(TcShape<D, BS>::NW * 32, 1)
         const int st = i % STAGES;
         uint64_t* bar = wbar + st;
         const int32_t blk = __ldg(p.block_table + static_cast<int64_t>(pc.req) * p.max_blocks + pc.pp);
+        // published to the consumer lanes by the barrier's release/acquire
+        stage_blk[warp * STAGES + st] = (blk < 0 || blk >= p.num_blocks) ? -1 : blk;
         if (blk < 0 || blk >= p.num_blocks) {
             set_err(p.err, YOCO_DEVERR_PAGE_RANGE);
             mbar_arrive(bar);
@@ -309,8 +322,7 @@ __global__ void __launch_bounds__(TcShape<D, BS>::NW * 32, 1)
             break;
         }
         consumed = i + 1;
-        const int32_t blk = __ldg(p.block_table + static_cast<int64_t>(cc.req) * p.max_blocks + cc.pp);
-        if (blk >= 0 && blk < p.num_blocks) {
+        if (stage_blk[warp * STAGES + st] >= 0) {
             const uint32_t kbase = smem_u32(wbuf + st * S::STAGE_BYTES);
             const uint32_t vbase = kbase + S::PAGE_BYTES;
             const int32_t nvalid = min(BS, cc.kv_len - cc.pp * BS);
