@@ -183,6 +183,13 @@ yoco_status_t yoco_set_l2_window(void* stream, void* base, size_t bytes, float h
 /* Human-readable name of a status code (static string). */
 const char* yoco_status_string(yoco_status_t status);
 
+/*
+ * The cudaError_t behind the most recent YOCO_ERR_CUDA returned on the
+ * calling thread (0 if none yet), and its description (static string).
+ */
+int32_t yoco_last_cuda_error(void);
+const char* yoco_last_cuda_error_string(void);
+
 /* Library version as major * 10000 + minor * 100 + patch. */
 int32_t yoco_version(void);
 

@@ -51,6 +51,7 @@ def test_status_strings_and_version(lib_path):
     assert N.status_name(0) == "ok"
     assert "workspace" in N.status_name(3)
     assert N.yoco_version() == 100
+    assert N.yoco_last_cuda_error() == 0  # nothing has failed on this thread
 
 
 def test_host_validation_rejects_before_launch(lib_path):

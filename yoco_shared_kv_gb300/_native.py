@@ -26,12 +26,16 @@ DEVERR_OFFSETS = 0x8
 DEVERR_TIMEOUT = 0x10
 
 EXPORTED = ("yoco_kv_append", "yoco_select_cross_rows", "yoco_cross_attn_workspace_size",
-            "yoco_cross_attn_paged", "yoco_set_l2_window", "yoco_status_string", "yoco_version")
+            "yoco_cross_attn_paged", "yoco_set_l2_window", "yoco_status_string", "yoco_version",
+            "yoco_last_cuda_error", "yoco_last_cuda_error_string")
 
 
 class YocoError(RuntimeError):
     def __init__(self, fn: str, status: int):
-        super().__init__(f"{fn} failed: {status_name(status)} (status {status})")
+        msg = f"{fn} failed: {status_name(status)} (status {status})"
+        if status == YOCO_ERR_CUDA:
+            msg += f": {lib.yoco_last_cuda_error_string().decode()}"
+        super().__init__(msg)
         self.status = status
 
 
@@ -57,6 +61,10 @@ def _load() -> ctypes.CDLL:
     L.yoco_status_string.argtypes = [ctypes.c_int]
     L.yoco_version.restype = ctypes.c_int32
     L.yoco_version.argtypes = []
+    L.yoco_last_cuda_error.restype = ctypes.c_int32
+    L.yoco_last_cuda_error.argtypes = []
+    L.yoco_last_cuda_error_string.restype = ctypes.c_char_p
+    L.yoco_last_cuda_error_string.argtypes = []
     return L
 
 
@@ -172,3 +180,11 @@ def yoco_set_l2_window(base: Optional[torch.Tensor], nbytes: int, hit_ratio: flo
 
 def yoco_version() -> int:
     return int(lib.yoco_version())
+
+
+def yoco_last_cuda_error() -> int:
+    return int(lib.yoco_last_cuda_error())
+
+
+def yoco_last_cuda_error_string() -> str:
+    return lib.yoco_last_cuda_error_string().decode()

@@ -14,6 +14,23 @@ extern "C" const char* yoco_status_string(yoco_status_t status) {
 
 extern "C" int32_t yoco_version(void) { return 100; }  // 0.1.0
 
+namespace yoco {
+namespace {
+thread_local int g_last_cuda_error = 0;
+}
+yoco_status_t cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return YOCO_OK;
+    g_last_cuda_error = static_cast<int>(e);
+    return YOCO_ERR_CUDA;
+}
+}  // namespace yoco
+
+extern "C" int32_t yoco_last_cuda_error(void) { return yoco::g_last_cuda_error; }
+
+extern "C" const char* yoco_last_cuda_error_string(void) {
+    return cudaGetErrorString(static_cast<cudaError_t>(yoco::g_last_cuda_error));
+}
+
 // The serial cross-decoder layers re-read one shared cache ("YOCO
 // 论文与推理数据流详解" §11); when the cache (or its hot part) fits in L2,
 // a persisting access-policy window keeps it there between layers.

@@ -176,19 +176,36 @@ __device__ __forceinline__ int32_t owner(int64_t x, int64_t P, int32_t workers) 
     return static_cast<int32_t>(((x + 1) * workers - 1) / P);
 }
 
+// Most CTAs one merge can span (the grid has one CTA per SM).
+constexpr int kMaxMergePieces = 1024;
+
 struct PieceHdr {
     int64_t s0, s1;  // segment [first page, end) in the flattened order
     int32_t n, g;
     int32_t valid;
 };
 
-// Workspace carve-up (floats): warp pieces then CTA pieces, outputs then stats.
+// The segment holding a CTA's first page, as seen by that CTA (read by the
+// merge kernel, so it needs no scan of the metadata of its own).
+struct CtaHdr {
+    int64_t P;       // pages of the launch
+    int64_t s0, s1;  // segment [first page, end); s0 < 0 when the CTA's start is past the end
+    int32_t n, g;
+};
+
+// Workspace carve-up: [W + C][2][G][D] partial outputs (warp pieces, then CTA
+// pieces), [W + C][2][G] (m, l), then one header per CTA.
 struct TcWs {
     float* w_o;
     float* c_o;
     float2* w_ml;
     float2* c_ml;
+    CtaHdr* hdr;
 };
+
+__host__ __device__ __forceinline__ int64_t tc_pieces(int64_t ctas, int nw, int G) {
+    return (ctas * nw + ctas) * 2 * G;
+}
 
 __device__ __forceinline__ TcWs tc_ws(const AttnParams& p, int ctas, int nw, int D) {
     TcWs w;
@@ -198,6 +215,7 @@ __device__ __forceinline__ TcWs tc_ws(const AttnParams& p, int ctas, int nw, int
     w.c_o = p.ws_o + W * per * D;
     w.w_ml = p.ws_ml;
     w.c_ml = p.ws_ml + W * per;
+    w.hdr = reinterpret_cast<CtaHdr*>(p.ws_ml + tc_pieces(ctas, nw, p.G));
     return w;
 }
 
@@ -209,6 +227,8 @@ __global__ void __launch_bounds__(TcShape<D, BS>::NW * 32, 1)
                        const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
     using S = TcShape<D, BS>;
     constexpr int NW = S::NW, STAGES = S::STAGES;
+    static_assert(2 * 16 * (D * 4 + 8) <= STAGES * S::STAGE_BYTES,
+                  "a warp's two end-of-slice pieces must fit in its ring");
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bars[NW * STAGES];
     __shared__ int32_t stage_blk[NW * STAGES];  // physical page of each stage (-1: invalid)
@@ -248,6 +268,19 @@ __global__ void __launch_bounds__(TcShape<D, BS>::NW * 32, 1)
     Cursor cc;  // page being consumed
     cc.req = -1;
     if (n_my > 0) locate(p, lane, my_lo, cap, cc);
+    if (warp == 0) {  // header for the merge kernel: the segment of page cta_lo
+        Cursor h0 = cc;
+        if (n_my <= 0 && cta_lo < P) locate(p, lane, cta_lo, cap, h0);
+        if (lane == 0) {
+            CtaHdr hd;
+            hd.P = P;
+            hd.s0 = (cta_lo < P && h0.req >= 0) ? h0.seg_start : -1;
+            hd.s1 = hd.s0 >= 0 ? h0.seg_start + h0.pages : -1;
+            hd.n = h0.n;
+            hd.g = h0.g;
+            ws.hdr[blockIdx.x] = hd;
+        }
+    }
     Cursor pc = cc;  // next page to issue (lane 0)
 
     auto issue = [&](int i) {  // lane 0 only; pc is at page i
@@ -312,7 +345,9 @@ __global__ void __launch_bounds__(TcShape<D, BS>::NW * 32, 1)
     reset_state();
     const float sl2 = p.scale_log2;
     bool aborted = false;
+    bool reload_first = false;  // this warp's first-segment piece sits in global memory
     int consumed = 0;
+    const int piece_bytes = p.G * (D * 4 + 8);  // one piece: [G][D] o, then [G] (m, l)
 
     for (int i = 0; i < n_my; ++i) {
         if (i == 0 || cc.pp == 0) load_q(cc.n, cc.g);
@@ -478,20 +513,35 @@ __global__ void __launch_bounds__(TcShape<D, BS>::NW * 32, 1)
                     }
             } else {
                 const int slot = s0 < my_lo ? 0 : 1;
-                const int64_t piece = (static_cast<int64_t>(wid) * 2 + slot) * p.G;
+                // A piece flushed at the end of the slice goes to this warp's
+                // ring, idle from here on; the one flushed mid-stream (the
+                // warp's first segment) goes to global memory and is brought
+                // back into the ring after streaming.
+                const bool at_end = (i == n_my - 1);
+                float* dst_o;
+                float2* dst_ml;
+                if (at_end) {
+                    dst_o = reinterpret_cast<float*>(wbuf + slot * piece_bytes);
+                    dst_ml = reinterpret_cast<float2*>(dst_o + p.G * D);
+                } else {
+                    const int64_t piece = (static_cast<int64_t>(wid) * 2 + slot) * p.G;
+                    dst_o = ws.w_o + piece * D;
+                    dst_ml = ws.w_ml + piece;
+                    reload_first = true;
+                }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int h = nt * 8 + 2 * tq + e;
                         if (h >= p.G) continue;
-                        float* dst = ws.w_o + (piece + h) * D;
+                        float* dst = dst_o + h * D;
 #pragma unroll
                         for (int md = 0; md < S::KD; ++md) {
                             dst[md * 16 + gl] = o[md][nt][e];
                             dst[md * 16 + gl + 8] = o[md][nt][2 + e];
                         }
-                        if (gl == 0) ws.w_ml[piece + h] = make_float2(m_run[nt][e], l_part[nt][e]);
+                        if (gl == 0) dst_ml[h] = make_float2(m_run[nt][e], l_part[nt][e]);
                     }
                 if (lane == 0) {
                     hdr[warp][slot].s0 = s0;
@@ -516,11 +566,28 @@ __global__ void __launch_bounds__(TcShape<D, BS>::NW * 32, 1)
             atomicExch(&abort_flag, 1);
         }
     }
-    __syncthreads();  // warp pieces are in global memory, headers in shared memory
+    // the merge kernel may be scheduled now; it waits for this grid to finish
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (reload_first && !aborted) {
+        // bring the mid-stream piece (slot 0) back next to the slice-end one
+        const int64_t piece = static_cast<int64_t>(wid) * 2 * p.G;
+        const float4* src = reinterpret_cast<const float4*>(ws.w_o + piece * D);
+        float4* dst = reinterpret_cast<float4*>(wbuf);
+        for (int v = lane; v < p.G * D / 4; v += 32) dst[v] = src[v];
+        float2* dml = reinterpret_cast<float2*>(reinterpret_cast<float*>(wbuf) + p.G * D);
+        for (int h = lane; h < p.G; h += 32) dml[h] = ws.w_ml[piece + h];
+    }
+    __syncthreads();  // pieces are in the warps' rings, headers in shared memory
     if (abort_flag) return;
 
     // ---- combine the pieces of each segment this CTA holds, in warp order ----
+    __shared__ float fac[2 * NW][16];  // per piece and head: 2^(m - M) (/ L for an output)
+    __shared__ float2 seg_ml[16];      // per head: (M, L) of the combined piece
     __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out);
+    auto piece_o = [&](int e) {
+        return reinterpret_cast<const float*>(smem + (e >> 1) * STAGES * S::STAGE_BYTES +
+                                              (e & 1) * piece_bytes);
+    };
     int e0 = 0;  // index into the flattened (warp, slot) header list
     while (e0 < 2 * NW) {
         if (!hdr[e0 >> 1][e0 & 1].valid) {
@@ -535,34 +602,45 @@ __global__ void __launch_bounds__(TcShape<D, BS>::NW * 32, 1)
             ++e1;
         }
         const bool whole = H.s0 >= cta_lo && H.s1 <= cta_hi;
+        if (threadIdx.x < p.G) {  // one thread per head builds the scale table
+            const int h = threadIdx.x;
+            float M = -INFINITY;
+            for (int e = e0; e < e1; ++e)
+                if (hdr[e >> 1][e & 1].valid)
+                    M = fmaxf(M, reinterpret_cast<const float2*>(piece_o(e) + p.G * D)[h].x);
+            float L = 0.f;
+            for (int e = e0; e < e1; ++e) {
+                float f = 0.f;
+                if (hdr[e >> 1][e & 1].valid) {
+                    const float2 ml = reinterpret_cast<const float2*>(piece_o(e) + p.G * D)[h];
+                    if (ml.x != -INFINITY) f = exp2_approx(ml.x - M);
+                    L += ml.y * f;
+                }
+                fac[e][h] = f;
+            }
+            if (whole) {
+                const float inv = 1.f / L;
+                for (int e = e0; e < e1; ++e) fac[e][h] *= inv;
+            }
+            seg_ml[h] = make_float2(M, L);
+        }
+        __syncthreads();
         const int cslot = H.s0 < cta_lo ? 0 : 1;
         const int64_t head0 = static_cast<int64_t>(H.n) * p.H_q + H.g * p.G;
         for (int idx = threadIdx.x; idx < p.G * D; idx += blockDim.x) {
-            const int h = idx / D, d = idx - (idx / D) * D;
-            float M = -INFINITY;
-            for (int e = e0; e < e1; ++e) {
-                if (!hdr[e >> 1][e & 1].valid) continue;
-                const int64_t pc_ = (static_cast<int64_t>(blockIdx.x * NW + (e >> 1)) * 2 + (e & 1)) * p.G;
-                M = fmaxf(M, ws.w_ml[pc_ + h].x);
-            }
-            float L = 0.f, O = 0.f;
-            for (int e = e0; e < e1; ++e) {
-                if (!hdr[e >> 1][e & 1].valid) continue;
-                const int64_t pc_ = (static_cast<int64_t>(blockIdx.x * NW + (e >> 1)) * 2 + (e & 1)) * p.G;
-                const float2 ml = ws.w_ml[pc_ + h];
-                if (ml.x == -INFINITY) continue;
-                const float f = exp2_approx(ml.x - M);
-                L += ml.y * f;
-                O += ws.w_o[(pc_ + h) * D + d] * f;
-            }
+            const int h = idx / D;
+            float O = 0.f;
+            for (int e = e0; e < e1; ++e)  // unused slots may hold stale bytes: skip, never scale by 0
+                if (hdr[e >> 1][e & 1].valid) O += piece_o(e)[idx] * fac[e][h];
             if (whole) {
-                outp[(head0 + h) * D + d] = __float2bfloat16_rn(O / L);
+                outp[head0 * D + idx] = __float2bfloat16_rn(O);
             } else {
                 const int64_t cp = (static_cast<int64_t>(blockIdx.x) * 2 + cslot) * p.G + h;
-                ws.c_o[cp * D + d] = O;
-                if (d == 0) ws.c_ml[cp] = make_float2(M, L);
+                ws.c_o[cp * D + (idx - h * D)] = O;
+                if (idx - h * D == 0) ws.c_ml[cp] = seg_ml[h];
             }
         }
+        __syncthreads();  // the scale table is rewritten for the next group
         e0 = e1;
     }
 }
@@ -578,6 +656,8 @@ __global__ void __launch_bounds__(D) attn_tc_merge(const AttnParams p, int32_t c
     const int64_t cap64 = static_cast<int64_t>(p.max_blocks) * p.block_size;
     const int32_t cap = cap64 > 0x7fffffff ? 0x7fffffff : static_cast<int32_t>(cap64);
     __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out);
+    // launched as a programmatic dependent of attn_tc_persistent: wait for it
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // rows with no key to attend: zero output, flag (rows spread over the CTAs)
     if (h == 0 && p.num_reqs > 0) {
@@ -597,18 +677,13 @@ __global__ void __launch_bounds__(D) attn_tc_merge(const AttnParams p, int32_t c
     if (launch_aborted(p)) return;
     if (c == 0) return;  // CTA 0's start is never strictly inside a segment
 
-    // the segment holding this CTA's first page (all warps compute it)
-    const int64_t P = total_pages(p, lane, cap);
-    const int64_t lo = P * c / ctas;
-    if (lo >= P) return;
-    Cursor cur;
-    locate(p, lane, lo, cap, cur);
-    if (cur.req < 0) return;
-    const int64_t s0 = cur.seg_start, s1 = cur.seg_start + cur.pages;
+    const TcWs ws = tc_ws(p, ctas, NW, D);
+    const CtaHdr H = ws.hdr[c];
+    if (H.s0 < 0) return;
+    const int64_t P = H.P, s0 = H.s0, s1 = H.s1;
     const int32_t c_first = owner(s0, P, ctas);
     if (c != c_first + 1) return;  // only the first CTA starting inside the segment merges
     const int32_t c_last = owner(s1 - 1, P, ctas);
-    const TcWs ws = tc_ws(p, ctas, NW, D);
     // A CTA keeps slot 0 for a segment that began before its slice and slot 1
     // for one that begins inside it; only c_first holds the segment's start.
     auto piece_of = [&](int32_t cc_) -> int64_t {
@@ -616,53 +691,105 @@ __global__ void __launch_bounds__(D) attn_tc_merge(const AttnParams p, int32_t c
         return (static_cast<int64_t>(cc_) * 2 + slot) * p.G + h;
     };
     auto nonempty = [&](int32_t cc_) { return P * cc_ / ctas < P * (cc_ + 1) / ctas; };
-    if (warp == 0) {
+    // scale factor per CTA piece: 2^(m - M) / L (0 for an empty CTA or piece)
+    __shared__ float fac[kMaxMergePieces];
+    __shared__ float red[D / 32];
+    const int np = c_last - c_first + 1;
+    float mx = -INFINITY;
+    for (int i = threadIdx.x; i < np; i += D)
+        if (nonempty(c_first + i)) mx = fmaxf(mx, ws.c_ml[piece_of(c_first + i)].x);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (lane == 0) red[warp] = mx;
+    __syncthreads();
+    if (threadIdx.x == 0) {
         float M = -INFINITY;
-        for (int32_t cc_ = c_first + lane; cc_ <= c_last; cc_ += 32)
-            if (nonempty(cc_)) M = fmaxf(M, ws.c_ml[piece_of(cc_)].x);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-        float L = 0.f;
-        for (int32_t cc_ = c_first + lane; cc_ <= c_last; cc_ += 32)
-            if (nonempty(cc_)) {
-                const float2 ml = ws.c_ml[piece_of(cc_)];
-                if (ml.x != -INFINITY) L += ml.y * exp2_approx(ml.x - M);
-            }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-        if (lane == 0) {
-            sM = M;
-            sL = L;
-        }
+        for (int w = 0; w < D / 32; ++w) M = fmaxf(M, red[w]);
+        sM = M;
     }
     __syncthreads();
-    const float M = sM, invL = 1.f / sL;
-    const int d = threadIdx.x;
-    float acc = 0.f;
-    for (int32_t cc_ = c_first; cc_ <= c_last; ++cc_) {
-        if (!nonempty(cc_)) continue;
-        const int64_t pc_ = piece_of(cc_);
-        const float2 ml = ws.c_ml[pc_];
-        if (ml.x == -INFINITY) continue;
-        acc += ws.c_o[pc_ * D + d] * exp2_approx(ml.x - M);
+    const float M = sM;
+    float lsum = 0.f;
+    for (int i = threadIdx.x; i < np; i += D) {
+        float f = 0.f;
+        if (nonempty(c_first + i)) {
+            const float2 ml = ws.c_ml[piece_of(c_first + i)];
+            if (ml.x != -INFINITY) f = exp2_approx(ml.x - M);
+            lsum += ml.y * f;
+        }
+        fac[i] = f;
     }
-    const int64_t head = static_cast<int64_t>(cur.n) * p.H_q + cur.g * p.G + h;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+    __syncthreads();
+    if (lane == 0) red[warp] = lsum;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float L = 0.f;
+        for (int w = 0; w < D / 32; ++w) L += red[w];
+        sL = L;
+    }
+    __syncthreads();
+    const float invL = 1.f / sL;
+    const int d = threadIdx.x;
+    const float* base = ws.c_o + (static_cast<int64_t>(c_first) * 2 * p.G + h) * D + d;
+    // piece i lives at CTA c_first + i, slot 1 for i == 0 and 0 otherwise
+    // an empty CTA's slot was never written (stale, maybe NaN): select, never scale by 0
+    auto term = [&](float a, float f) { return f != 0.f ? a * f : 0.f; };
+    const int64_t st = static_cast<int64_t>(2) * p.G * D;
+    float acc = term(base[static_cast<int64_t>(p.G) * D], fac[0]);
+    int i = 1;
+    for (; i + 4 <= np; i += 4) {
+        const float a0 = base[st * (i + 0)], a1 = base[st * (i + 1)];
+        const float a2 = base[st * (i + 2)], a3 = base[st * (i + 3)];
+        acc += term(a0, fac[i]) + term(a1, fac[i + 1]) + term(a2, fac[i + 2]) + term(a3, fac[i + 3]);
+    }
+    for (; i < np; ++i) acc += term(base[st * i], fac[i]);
+    const int64_t head = static_cast<int64_t>(H.n) * p.H_q + H.g * p.G + h;
     outp[head * D + d] = __float2bfloat16_rn(acc * invL);
+}
+
+// One-time (per device) setting of a kernel's dynamic shared memory limit.
+// `done` must be distinct per kernel: callers keep it in a function that is
+// itself instantiated per kernel.
+template <typename K>
+cudaError_t ensure_smem_attr(K kernel, int bytes, unsigned long long& done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = dev < 64 ? (1ull << dev) : 0;
+    if (bit && (__atomic_load_n(&done, __ATOMIC_ACQUIRE) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) __atomic_fetch_or(&done, bit, __ATOMIC_RELEASE);
+    return e;
 }
 
 template <int D, int BS, int NT>
 cudaError_t launch_one(const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p, int sms,
                        cudaStream_t s) {
     using S = TcShape<D, BS>;
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_persistent<D, BS, NT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+    static unsigned long long smem_set = 0;  // one flag word per kernel instantiation
+    cudaError_t e = ensure_smem_attr(attn_tc_persistent<D, BS, NT>, S::SMEM, smem_set);
     if (e != cudaSuccess) return e;
     const int ctas = tc_ctas(sms);
-    attn_tc_persistent<D, BS, NT><<<ctas, S::NW * 32, S::SMEM, s>>>(mk, mv, p);
+    AttnParams q = p;  // workspace: outputs of all pieces, then their (m, l), then headers
+    q.ws_ml = reinterpret_cast<float2*>(p.ws_o + tc_pieces(ctas, S::NW, p.G) * D);
+    attn_tc_persistent<D, BS, NT><<<ctas, S::NW * 32, S::SMEM, s>>>(mk, mv, q);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    attn_tc_merge<D, S::NW><<<dim3(ctas, p.G), D, 0, s>>>(p, ctas);
-    return cudaGetLastError();
+    // programmatic dependent launch: the merge grid is scheduled while the
+    // split grid drains and waits on it with griddepcontrol.wait
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctas, p.G);
+    cfg.blockDim = dim3(D);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_tc_merge<D, S::NW>, q, static_cast<int32_t>(ctas));
 }
 
 template <int D>
@@ -687,13 +814,13 @@ int tc_nw(int D, int BS) {
 
 }  // namespace
 
-int tc_ctas(int sms) { return sms; }
+int tc_ctas(int sms) { return sms < kMaxMergePieces ? sms : kMaxMergePieces; }
 
 size_t tc_workspace_bytes(int sms, int H_kv, int G, int D, int BS) {
     (void)H_kv;
-    const size_t ctas = static_cast<size_t>(tc_ctas(sms));
-    const size_t W = ctas * tc_nw(D, BS);
-    return (W + ctas) * 2 * static_cast<size_t>(G) * (static_cast<size_t>(D) * 4 + 8);
+    const int64_t ctas = tc_ctas(sms);
+    const size_t pieces = static_cast<size_t>(tc_pieces(ctas, tc_nw(D, BS), G));
+    return pieces * (static_cast<size_t>(D) * 4 + 8) + static_cast<size_t>(ctas) * sizeof(CtaHdr);
 }
 
 cudaError_t launch_attn_tc(const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p,

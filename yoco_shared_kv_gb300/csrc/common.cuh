@@ -16,10 +16,14 @@ namespace yoco {
 
 // ---------------------------------------------------------------- host side
 
-#define YOCO_CUDA_OK(expr)                          \
-    do {                                            \
-        cudaError_t e_ = (expr);                    \
-        if (e_ != cudaSuccess) return YOCO_ERR_CUDA; \
+// Maps a CUDA runtime result to a status, remembering a failure for
+// yoco_last_cuda_error() on this thread.
+yoco_status_t cuda_status(cudaError_t e);
+
+#define YOCO_CUDA_OK(expr)                                \
+    do {                                                  \
+        cudaError_t e_ = (expr);                          \
+        if (e_ != cudaSuccess) return yoco::cuda_status(e_); \
     } while (0)
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

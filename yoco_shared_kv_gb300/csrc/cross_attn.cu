@@ -92,6 +92,43 @@ bool encode_pool(CUtensorMap* map, const void* pool, int64_t rows, int D, int BS
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Small cache of encoded pool descriptors: the pools of a serving engine are
+// fixed, so each is encoded once instead of on every call.
+bool pool_map(CUtensorMap* map, const void* pool, int64_t rows, int D, int BS) {
+    struct Entry {
+        const void* pool;
+        int64_t rows;
+        int D, BS, dev;
+        CUtensorMap map;
+    };
+    static Entry cache[16];
+    static int used = 0, next = 0;
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < used; ++i)
+            if (cache[i].pool == pool && cache[i].rows == rows && cache[i].D == D &&
+                cache[i].BS == BS && cache[i].dev == dev) {
+                *map = cache[i].map;
+                return true;
+            }
+    }
+    if (!encode_pool(map, pool, rows, D, BS)) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    Entry& e = cache[next];
+    e.pool = pool;
+    e.rows = rows;
+    e.D = D;
+    e.BS = BS;
+    e.dev = dev;
+    e.map = *map;
+    next = (next + 1) % 16;
+    if (used < 16) ++used;
+    return true;
+}
+
 }  // namespace
 
 int device_sm_count() {
@@ -167,16 +204,13 @@ extern "C" yoco_status_t yoco_cross_attn_paged(
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (pl.tc) {
-        // workspace: [pieces][G][D] partial outputs, then [pieces][G] (m, l)
-        const size_t pieces_x_g = pl.ws_bytes / (static_cast<size_t>(head_dim) * 4 + 8);
-        p.ws_o = static_cast<float*>(workspace);
-        p.ws_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) +
-                                            pieces_x_g * head_dim * 4);
+        p.ws_o = static_cast<float*>(workspace);  // carved up by the launcher
+        p.ws_ml = nullptr;
         CUtensorMap mk, mv;
         const int64_t rows = static_cast<int64_t>(num_blocks) * num_kv_heads * block_size;
-        if (!encode_pool(&mk, k_cache, rows, head_dim, block_size) ||
-            !encode_pool(&mv, v_cache, rows, head_dim, block_size))
-            return YOCO_ERR_CUDA;
+        if (!pool_map(&mk, k_cache, rows, head_dim, block_size) ||
+            !pool_map(&mv, v_cache, rows, head_dim, block_size))
+            return cuda_status(cudaErrorInvalidValue);  // descriptor encoding refused
         e = launch_attn_tc(mk, mv, p, head_dim, block_size, device_sm_count(), s);
     } else {
         p.ws_o = static_cast<float*>(workspace);
@@ -187,5 +221,5 @@ extern "C" yoco_status_t yoco_cross_attn_paged(
                       : nullptr;
         e = launch_attn_cc(k_cache, v_cache, p, head_dim, pl.hb, s);
     }
-    return e == cudaSuccess ? YOCO_OK : YOCO_ERR_CUDA;
+    return cuda_status(e);
 }

@@ -140,5 +140,5 @@ extern "C" yoco_status_t yoco_kv_append(const void* k_new, const void* v_new, vo
             break;
         default: return YOCO_ERR_UNSUPPORTED;
     }
-    return e == cudaSuccess ? YOCO_OK : YOCO_ERR_CUDA;
+    return cuda_status(e);
 }

@@ -90,5 +90,5 @@ extern "C" yoco_status_t yoco_select_cross_rows(const int32_t* query_start_loc,
     select_rows_kernel<<<1, kSelectThreads, 0, static_cast<cudaStream_t>(stream)>>>(
         query_start_loc, rows_per_req, num_reqs, row_indices, cross_query_start_loc, num_rows,
         err_word);
-    return cudaGetLastError() == cudaSuccess ? YOCO_OK : YOCO_ERR_CUDA;
+    return cuda_status(cudaGetLastError());
 }
