@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(TcShape<D, BS>::NW * 32, 1)
                        const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
     using S = TcShape<D, BS>;
     constexpr int NW = S::NW, STAGES = S::STAGES;
-    static_assert(2 * 16 * (D * 4 + 8) <= STAGES * S::STAGE_BYTES,
+    static_assert(2 * (16 * (D * 4 + 8) + 16) <= STAGES * S::STAGE_BYTES,
                   "a warp's two end-of-slice pieces must fit in its ring");
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bars[NW * STAGES];
@@ -268,18 +268,15 @@ __global__ void __launch_bounds__(TcShape<D, BS>::NW * 32, 1)
     Cursor cc;  // page being consumed
     cc.req = -1;
     if (n_my > 0) locate(p, lane, my_lo, cap, cc);
-    if (warp == 0) {  // header for the merge kernel: the segment of page cta_lo
+    CtaHdr hd;  // header for the merge kernel: the segment of page cta_lo (warp 0)
+    if (warp == 0) {
         Cursor h0 = cc;
         if (n_my <= 0 && cta_lo < P) locate(p, lane, cta_lo, cap, h0);
-        if (lane == 0) {
-            CtaHdr hd;
-            hd.P = P;
-            hd.s0 = (cta_lo < P && h0.req >= 0) ? h0.seg_start : -1;
-            hd.s1 = hd.s0 >= 0 ? h0.seg_start + h0.pages : -1;
-            hd.n = h0.n;
-            hd.g = h0.g;
-            ws.hdr[blockIdx.x] = hd;
-        }
+        hd.P = P;
+        hd.s0 = (cta_lo < P && h0.req >= 0) ? h0.seg_start : -1;
+        hd.s1 = hd.s0 >= 0 ? h0.seg_start + h0.pages : -1;
+        hd.n = h0.n;
+        hd.g = h0.g;
     }
     Cursor pc = cc;  // next page to issue (lane 0)
 
@@ -309,6 +306,11 @@ __global__ void __launch_bounds__(TcShape<D, BS>::NW * 32, 1)
         const int pro = n_my < STAGES ? n_my : STAGES;
         for (int i = 0; i < pro; ++i) issue(i);
     }
+    // Launched as a programmatic dependent of the previous kernel in the
+    // stream: everything above only reads the (unchanging) metadata and the
+    // cache. Queries, outputs and the workspace are touched after this wait.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (warp == 0 && lane == 0) ws.hdr[blockIdx.x] = hd;
 
     uint32_t qf[S::KD][NT][2];
     float o[S::KD][NT][4];
@@ -347,7 +349,8 @@ __global__ void __launch_bounds__(TcShape<D, BS>::NW * 32, 1)
     bool aborted = false;
     bool reload_first = false;  // this warp's first-segment piece sits in global memory
     int consumed = 0;
-    const int piece_bytes = p.G * (D * 4 + 8);  // one piece: [G][D] o, then [G] (m, l)
+    // one piece: [G][D] o, then [G] (m, l); 16-byte stride keeps float4 access aligned
+    const int piece_bytes = (p.G * (D * 4 + 8) + 15) & ~15;
 
     for (int i = 0; i < n_my; ++i) {
         if (i == 0 || cc.pp == 0) load_q(cc.n, cc.g);
@@ -566,14 +569,21 @@ __global__ void __launch_bounds__(TcShape<D, BS>::NW * 32, 1)
             atomicExch(&abort_flag, 1);
         }
     }
-    // the merge kernel may be scheduled now; it waits for this grid to finish
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (reload_first && !aborted) {
         // bring the mid-stream piece (slot 0) back next to the slice-end one
         const int64_t piece = static_cast<int64_t>(wid) * 2 * p.G;
         const float4* src = reinterpret_cast<const float4*>(ws.w_o + piece * D);
         float4* dst = reinterpret_cast<float4*>(wbuf);
-        for (int v = lane; v < p.G * D / 4; v += 32) dst[v] = src[v];
+        const int nv = p.G * D / 4;
+        for (int v0 = lane; v0 < nv; v0 += 32 * 8) {  // 8 loads in flight per lane
+            float4 r[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (v0 + u * 32 < nv) r[u] = src[v0 + u * 32];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (v0 + u * 32 < nv) dst[v0 + u * 32] = r[u];
+        }
         float2* dml = reinterpret_cast<float2*>(reinterpret_cast<float*>(wbuf) + p.G * D);
         for (int h = lane; h < p.G; h += 32) dml[h] = ws.w_ml[piece + h];
     }
@@ -581,68 +591,89 @@ __global__ void __launch_bounds__(TcShape<D, BS>::NW * 32, 1)
     if (abort_flag) return;
 
     // ---- combine the pieces of each segment this CTA holds, in warp order ----
-    __shared__ float fac[2 * NW][16];  // per piece and head: 2^(m - M) (/ L for an output)
-    __shared__ float2 seg_ml[16];      // per head: (M, L) of the combined piece
+    // Groups are consecutive valid pieces of one segment (at most 2 * NW).
+    // Loops run to a fixed bound with predication so every load of a group
+    // is issued before the arithmetic that needs it.
+    constexpr int MAXE = 2 * NW;
+    __shared__ float fac[MAXE][16];  // per piece and head: 2^(m - M) (/ L for an output)
+    __shared__ float2 seg_ml[16];    // per head: (M, L) of the combined piece
     __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out);
-    auto piece_o = [&](int e) {
-        return reinterpret_cast<const float*>(smem + (e >> 1) * STAGES * S::STAGE_BYTES +
-                                              (e & 1) * piece_bytes);
+    auto piece_base = [&](int e) {   // e = warp * 2 + slot
+        return smem + (e >> 1) * STAGES * S::STAGE_BYTES + (e & 1) * piece_bytes;
     };
-    int e0 = 0;  // index into the flattened (warp, slot) header list
-    while (e0 < 2 * NW) {
+    int e0 = 0;
+    while (e0 < MAXE) {
         if (!hdr[e0 >> 1][e0 & 1].valid) {
             ++e0;
             continue;
         }
         const PieceHdr H = hdr[e0 >> 1][e0 & 1];
-        int e1 = e0 + 1;  // group = following headers up to the next other segment
-        while (e1 < 2 * NW) {
+        int ent[MAXE];  // the group's valid pieces, in order
+        int ne = 0, e1 = e0;
+        for (; e1 < MAXE; ++e1) {
             const PieceHdr& X = hdr[e1 >> 1][e1 & 1];
-            if (X.valid && X.s0 != H.s0) break;
-            ++e1;
+            if (!X.valid) continue;
+            if (X.s0 != H.s0) break;
+            ent[ne++] = e1;
         }
         const bool whole = H.s0 >= cta_lo && H.s1 <= cta_hi;
         if (threadIdx.x < p.G) {  // one thread per head builds the scale table
             const int h = threadIdx.x;
+            float2 ml[MAXE];
+#pragma unroll
+            for (int k = 0; k < MAXE; ++k)
+                ml[k] = k < ne ? reinterpret_cast<const float2*>(piece_base(ent[k]) + p.G * D * 4)[h]
+                               : make_float2(-INFINITY, 0.f);
             float M = -INFINITY;
-            for (int e = e0; e < e1; ++e)
-                if (hdr[e >> 1][e & 1].valid)
-                    M = fmaxf(M, reinterpret_cast<const float2*>(piece_o(e) + p.G * D)[h].x);
-            float L = 0.f;
-            for (int e = e0; e < e1; ++e) {
-                float f = 0.f;
-                if (hdr[e >> 1][e & 1].valid) {
-                    const float2 ml = reinterpret_cast<const float2*>(piece_o(e) + p.G * D)[h];
-                    if (ml.x != -INFINITY) f = exp2_approx(ml.x - M);
-                    L += ml.y * f;
-                }
-                fac[e][h] = f;
+#pragma unroll
+            for (int k = 0; k < MAXE; ++k) M = fmaxf(M, ml[k].x);
+            float f[MAXE], L = 0.f;
+#pragma unroll
+            for (int k = 0; k < MAXE; ++k) {
+                f[k] = ml[k].x != -INFINITY ? exp2_approx(ml[k].x - M) : 0.f;
+                L += ml[k].y * f[k];
             }
-            if (whole) {
-                const float inv = 1.f / L;
-                for (int e = e0; e < e1; ++e) fac[e][h] *= inv;
-            }
+            const float sc = whole ? 1.f / L : 1.f;
+#pragma unroll
+            for (int k = 0; k < MAXE; ++k) fac[k][h] = f[k] * sc;
             seg_ml[h] = make_float2(M, L);
         }
         __syncthreads();
         const int cslot = H.s0 < cta_lo ? 0 : 1;
         const int64_t head0 = static_cast<int64_t>(H.n) * p.H_q + H.g * p.G;
-        for (int idx = threadIdx.x; idx < p.G * D; idx += blockDim.x) {
-            const int h = idx / D;
-            float O = 0.f;
-            for (int e = e0; e < e1; ++e)  // unused slots may hold stale bytes: skip, never scale by 0
-                if (hdr[e >> 1][e & 1].valid) O += piece_o(e)[idx] * fac[e][h];
+        const int nvec = p.G * D / 4;  // four consecutive elements (one head) per step
+        for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+            const int h = (v * 4) / D;
+            float4 x[MAXE];
+#pragma unroll
+            for (int k = 0; k < MAXE; ++k)
+                if (k < ne) x[k] = reinterpret_cast<const float4*>(piece_base(ent[k]))[v];
+            float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < MAXE; ++k)
+                if (k < ne) {
+                    const float fk = fac[k][h];
+                    O.x += x[k].x * fk;
+                    O.y += x[k].y * fk;
+                    O.z += x[k].z * fk;
+                    O.w += x[k].w * fk;
+                }
             if (whole) {
-                outp[head0 * D + idx] = __float2bfloat16_rn(O);
+                __nv_bfloat16* dst = outp + head0 * D + v * 4;
+                reinterpret_cast<__nv_bfloat162*>(dst)[0] = __floats2bfloat162_rn(O.x, O.y);
+                reinterpret_cast<__nv_bfloat162*>(dst)[1] = __floats2bfloat162_rn(O.z, O.w);
             } else {
                 const int64_t cp = (static_cast<int64_t>(blockIdx.x) * 2 + cslot) * p.G + h;
-                ws.c_o[cp * D + (idx - h * D)] = O;
-                if (idx - h * D == 0) ws.c_ml[cp] = seg_ml[h];
+                reinterpret_cast<float4*>(ws.c_o + cp * D)[(v * 4 - h * D) / 4] = O;
+                if (v * 4 - h * D == 0) ws.c_ml[cp] = seg_ml[h];
             }
         }
         __syncthreads();  // the scale table is rewritten for the next group
         e0 = e1;
     }
+    // the merge kernel may be scheduled now (it waits for this grid to finish);
+    // triggering only here keeps its waiting CTAs off the SM during the combine
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Combines the CTA-level partials of every segment cut by a CTA boundary
@@ -656,8 +687,10 @@ __global__ void __launch_bounds__(D) attn_tc_merge(const AttnParams p, int32_t c
     const int64_t cap64 = static_cast<int64_t>(p.max_blocks) * p.block_size;
     const int32_t cap = cap64 > 0x7fffffff ? 0x7fffffff : static_cast<int32_t>(cap64);
     __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out);
-    // launched as a programmatic dependent of attn_tc_persistent: wait for it
+    // launched as a programmatic dependent of attn_tc_persistent: wait for it,
+    // and let the next kernel (the next layer's split) start its prologue
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // rows with no key to attend: zero output, flag (rows spread over the CTAs)
     if (h == 0 && p.num_reqs > 0) {
@@ -693,10 +726,11 @@ __global__ void __launch_bounds__(D) attn_tc_merge(const AttnParams p, int32_t c
     auto nonempty = [&](int32_t cc_) { return P * cc_ / ctas < P * (cc_ + 1) / ctas; };
     // scale factor per CTA piece: 2^(m - M) / L (0 for an empty CTA or piece)
     __shared__ float fac[kMaxMergePieces];
-    __shared__ float red[D / 32];
+    constexpr int NT4 = D;  // one thread per output element
+    __shared__ float red[NT4 / 32];
     const int np = c_last - c_first + 1;
     float mx = -INFINITY;
-    for (int i = threadIdx.x; i < np; i += D)
+    for (int i = threadIdx.x; i < np; i += NT4)
         if (nonempty(c_first + i)) mx = fmaxf(mx, ws.c_ml[piece_of(c_first + i)].x);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
@@ -704,13 +738,13 @@ __global__ void __launch_bounds__(D) attn_tc_merge(const AttnParams p, int32_t c
     __syncthreads();
     if (threadIdx.x == 0) {
         float M = -INFINITY;
-        for (int w = 0; w < D / 32; ++w) M = fmaxf(M, red[w]);
+        for (int w = 0; w < NT4 / 32; ++w) M = fmaxf(M, red[w]);
         sM = M;
     }
     __syncthreads();
     const float M = sM;
     float lsum = 0.f;
-    for (int i = threadIdx.x; i < np; i += D) {
+    for (int i = threadIdx.x; i < np; i += NT4) {
         float f = 0.f;
         if (nonempty(c_first + i)) {
             const float2 ml = ws.c_ml[piece_of(c_first + i)];
@@ -726,23 +760,25 @@ __global__ void __launch_bounds__(D) attn_tc_merge(const AttnParams p, int32_t c
     __syncthreads();
     if (threadIdx.x == 0) {
         float L = 0.f;
-        for (int w = 0; w < D / 32; ++w) L += red[w];
+        for (int w = 0; w < NT4 / 32; ++w) L += red[w];
         sL = L;
     }
     __syncthreads();
     const float invL = 1.f / sL;
     const int d = threadIdx.x;
     const float* base = ws.c_o + (static_cast<int64_t>(c_first) * 2 * p.G + h) * D + d;
-    // piece i lives at CTA c_first + i, slot 1 for i == 0 and 0 otherwise
-    // an empty CTA's slot was never written (stale, maybe NaN): select, never scale by 0
+    // piece i lives at CTA c_first + i, slot 1 for i == 0 and 0 otherwise; an
+    // empty CTA's slot was never written (stale, maybe NaN): select, never scale by 0
     auto term = [&](float a, float f) { return f != 0.f ? a * f : 0.f; };
     const int64_t st = static_cast<int64_t>(2) * p.G * D;
     float acc = term(base[static_cast<int64_t>(p.G) * D], fac[0]);
     int i = 1;
-    for (; i + 4 <= np; i += 4) {
-        const float a0 = base[st * (i + 0)], a1 = base[st * (i + 1)];
-        const float a2 = base[st * (i + 2)], a3 = base[st * (i + 3)];
-        acc += term(a0, fac[i]) + term(a1, fac[i + 1]) + term(a2, fac[i + 2]) + term(a3, fac[i + 3]);
+    for (; i + 8 <= np; i += 8) {  // eight independent loads in flight
+        float a[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) a[u] = base[st * (i + u)];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) acc += term(a[u], fac[i + u]);
     }
     for (; i < np; ++i) acc += term(base[st * i], fac[i]);
     const int64_t head = static_cast<int64_t>(H.n) * p.H_q + H.g * p.G + h;
@@ -774,21 +810,26 @@ cudaError_t launch_one(const CUtensorMap& mk, const CUtensorMap& mv, const AttnP
     const int ctas = tc_ctas(sms);
     AttnParams q = p;  // workspace: outputs of all pieces, then their (m, l), then headers
     q.ws_ml = reinterpret_cast<float2*>(p.ws_o + tc_pieces(ctas, S::NW, p.G) * D);
-    attn_tc_persistent<D, BS, NT><<<ctas, S::NW * 32, S::SMEM, s>>>(mk, mv, q);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    // programmatic dependent launch: the merge grid is scheduled while the
-    // split grid drains and waits on it with griddepcontrol.wait
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(ctas, p.G);
-    cfg.blockDim = dim3(D);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = s;
+    // Both grids are programmatic dependents of the kernel before them: the
+    // split grid runs its metadata prologue while the previous kernel (for
+    // example the previous layer's merge) drains, and the merge grid is
+    // scheduled while the split grid drains; each waits (griddepcontrol.wait)
+    // before it touches data the previous grid produces.
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctas);
+    cfg.blockDim = dim3(S::NW * 32);
+    cfg.dynamicSmemBytes = S::SMEM;
+    cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, attn_tc_persistent<D, BS, NT>, mk, mv, q);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(ctas, p.G);
+    cfg.blockDim = dim3(D);
+    cfg.dynamicSmemBytes = 0;
     return cudaLaunchKernelEx(&cfg, attn_tc_merge<D, S::NW>, q, static_cast<int32_t>(ctas));
 }
 
