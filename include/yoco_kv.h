@@ -172,6 +172,44 @@ yoco_status_t yoco_cross_attn_paged(const void* q, const void* k_cache, const vo
                                     void* stream);
 
 /*
+ * yoco_cross_attn_paged_noalloc — yoco_cross_attn_paged for callers that
+ * cannot allocate device memory. The pages have no counterpart: this is a
+ * library convenience, not part of the method.
+ *
+ * Some callers cannot call cudaMalloc: code running while a CUDA graph is
+ * being captured, engines that carve out all device memory at start-up and
+ * forbid later allocations, and plugin hosts that expose no allocator. This
+ * entry point takes the same arguments as yoco_cross_attn_paged minus the
+ * workspace, and keeps its scratch in one fixed array inside the library
+ * (yoco_cross_attn_noalloc_capacity() bytes, 16 MiB), which every GPU that
+ * loads the library holds until the process exits. It allocates nothing and
+ * calls no allocating routine.
+ *   - Returns YOCO_ERR_WORKSPACE, before any launch, when these bounds need
+ *     more scratch than the array holds (yoco_cross_attn_workspace_size()
+ *     gives the need).
+ *   - The first call on each device looks up the array's device address
+ *     (with that device current); make that first call before any stream
+ *     capture on the device.
+ *   - Every call on a device shares the one array. The library writes each
+ *     scratch word before reading it within a call, so no clearing is
+ *     needed, but calls that overlap on the GPU (other streams, other host
+ *     threads) race on it: serialise them.
+ */
+yoco_status_t yoco_cross_attn_paged_noalloc(const void* q, const void* k_cache,
+                                            const void* v_cache, void* out,
+                                            const int32_t* block_table,
+                                            int32_t max_blocks_per_req, const int32_t* seq_lens,
+                                            const int32_t* cross_query_start_loc,
+                                            int32_t num_reqs, int32_t max_rows,
+                                            int32_t max_seq_len, int32_t num_q_heads,
+                                            int32_t num_kv_heads, int32_t head_dim,
+                                            int32_t block_size, int32_t num_blocks, float scale,
+                                            yoco_dtype_t dtype, int32_t* err_word, void* stream);
+
+/* Bytes of the fixed scratch array used by yoco_cross_attn_paged_noalloc. */
+size_t yoco_cross_attn_noalloc_capacity(void);
+
+/*
  * yoco_set_l2_window — mark [base, base + bytes) as persisting in L2 for
  * work later enqueued on `stream` (bytes == 0 clears the window). The L2
  * set-aside is a property of this process's CUDA context only. Used to

@@ -27,7 +27,8 @@ DEVERR_TIMEOUT = 0x10
 
 EXPORTED = ("yoco_kv_append", "yoco_select_cross_rows", "yoco_cross_attn_workspace_size",
             "yoco_cross_attn_paged", "yoco_set_l2_window", "yoco_status_string", "yoco_version",
-            "yoco_last_cuda_error", "yoco_last_cuda_error_string")
+            "yoco_last_cuda_error", "yoco_last_cuda_error_string",
+            "yoco_cross_attn_paged_noalloc", "yoco_cross_attn_noalloc_capacity")
 
 
 class YocoError(RuntimeError):
@@ -65,6 +66,12 @@ def _load() -> ctypes.CDLL:
     L.yoco_last_cuda_error.argtypes = []
     L.yoco_last_cuda_error_string.restype = ctypes.c_char_p
     L.yoco_last_cuda_error_string.argtypes = []
+    L.yoco_cross_attn_paged_noalloc.restype = ctypes.c_int
+    L.yoco_cross_attn_paged_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32,
+                                                i32, i32, i32, i32, i32, ctypes.c_float,
+                                                ctypes.c_int, vp, vp]
+    L.yoco_cross_attn_noalloc_capacity.restype = sz
+    L.yoco_cross_attn_noalloc_capacity.argtypes = []
     return L
 
 
@@ -170,6 +177,31 @@ def yoco_cross_attn_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch
         _i32(cross_query_start_loc, "cross_query_start_loc"), R, max_rows, int(max_seq_len), H_q,
         H_kv, D, bs, num_blocks, float(scale), dtype_code(q.dtype), _ptr(workspace), ws_bytes,
         None if err_word is None else _i32(err_word, "err_word"), _stream(stream)))
+
+
+def yoco_cross_attn_paged_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                  out: torch.Tensor, block_table: torch.Tensor,
+                                  seq_lens: torch.Tensor, cross_query_start_loc: torch.Tensor,
+                                  max_seq_len: int, scale: float,
+                                  err_word: Optional[torch.Tensor] = None, stream=None,
+                                  max_rows: Optional[int] = None) -> None:
+    """yoco_cross_attn_paged with the library's fixed scratch array: no workspace, no allocation."""
+    num_blocks, H_kv, bs, D = k_cache.shape
+    rows_cap, H_q, Dq = q.shape
+    assert Dq == D and out.shape == q.shape and out.dtype == q.dtype == k_cache.dtype
+    R = cross_query_start_loc.shape[0] - 1
+    max_rows = rows_cap if max_rows is None else max_rows
+    assert max_rows <= rows_cap
+    _check("yoco_cross_attn_paged_noalloc", lib.yoco_cross_attn_paged_noalloc(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _i32(block_table, "block_table"),
+        block_table.shape[1], _i32(seq_lens, "seq_lens"),
+        _i32(cross_query_start_loc, "cross_query_start_loc"), R, max_rows, int(max_seq_len), H_q,
+        H_kv, D, bs, num_blocks, float(scale), dtype_code(q.dtype),
+        None if err_word is None else _i32(err_word, "err_word"), _stream(stream)))
+
+
+def yoco_cross_attn_noalloc_capacity() -> int:
+    return int(lib.yoco_cross_attn_noalloc_capacity())
 
 
 def yoco_set_l2_window(base: Optional[torch.Tensor], nbytes: int, hit_ratio: float = 1.0,
