@@ -280,3 +280,30 @@ def test_workspace_too_small_is_rejected(P, N):
                                 ds.dev["block_table"], ds.dev["seq_lens"], ds.cqsl, 131072,
                                 wl.scale, ds.workspace[:16], dw.err)
     assert e.value.status == N.YOCO_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("lens,H_q,H_kv,D,bs", [([5], 8, 2, 256, 16), ([1, 3, 300], 8, 2, 128, 32),
+                                               ([40, 1, 17, 2000], 16, 1, 128, 32),
+                                               ([60000], 16, 1, 128, 32)])
+def test_attention_writes_only_its_outputs(P, N, lens, H_q, H_kv, D, bs):
+    """Canary regions around `out` stay untouched; scratch starts as NaN bytes."""
+    wl = pure_decode(3300 + len(lens), explicit_lens=lens, H_q=H_q, H_kv=H_kv, D=D, bs=bs,
+                     layers=1)
+    dw = P.DeviceWorkload(wl)
+    dw.run_fill()
+    dw.run_step(0)
+    torch.cuda.synchronize()
+    ds = dw.steps[0]
+    n_out = ds.out[0].numel()
+    pad = 4096
+    big = torch.full((pad + n_out + pad,), 7.0, dtype=torch.bfloat16, device="cuda")
+    out = big[pad:pad + n_out].view(ds.out[0].shape)
+    ds.workspace.fill_(255)
+    dw.attend(ds, 0, out=out)
+    torch.cuda.synchronize()
+    assert dw.error_bits() == 0
+    assert (big[:pad] == 7.0).all() and (big[pad + n_out:] == 7.0).all()
+    ref = oracle_step_out(wl, wl.steps[0])
+    got = gpu_out(out)[None]
+    assert np.isfinite(got).all()
+    assert np.abs(got - ref).max() <= ATOL["bf16"]

@@ -185,12 +185,14 @@ struct PieceHdr {
     int32_t valid;
 };
 
-// The segment holding a CTA's first page, as seen by that CTA (read by the
-// merge kernel, so it needs no scan of the metadata of its own).
+// The segments holding a CTA's first and last page, as seen by that CTA
+// (read by the merge kernel, so it needs no scan of the metadata itself).
 struct CtaHdr {
     int64_t P;       // pages of the launch
-    int64_t s0, s1;  // segment [first page, end); s0 < 0 when the CTA's start is past the end
-    int32_t n, g;
+    int64_t a0, a1;  // segment of the first page [first, end); a0 < 0: slice starts past the end
+    int64_t b0, b1;  // segment of the last page; b0 < 0: empty slice
+    int32_t an, ag;  // (row, kv head) of segment a
+    int32_t bn, bg;  // (row, kv head) of segment b
 };
 
 // Workspace carve-up: [W + C][2][G][D] partial outputs (warp pieces, then CTA
@@ -268,15 +270,21 @@ __global__ void __launch_bounds__(TcShape<D, BS>::NW * 32, 1)
     Cursor cc;  // page being consumed
     cc.req = -1;
     if (n_my > 0) locate(p, lane, my_lo, cap, cc);
-    CtaHdr hd;  // header for the merge kernel: the segment of page cta_lo (warp 0)
-    if (warp == 0) {
+    // header for the merge kernel: warp 0 finds the segment of page cta_lo,
+    // warp 1 the segment of page cta_hi - 1
+    int64_t hs0 = -1, hs1 = -1;
+    int32_t hn = 0, hg = 0;
+    if (warp <= 1) {
+        const int64_t x = warp == 0 ? cta_lo : cta_hi - 1;
+        const bool any = warp == 0 ? cta_lo < P : cta_hi > cta_lo;
         Cursor h0 = cc;
-        if (n_my <= 0 && cta_lo < P) locate(p, lane, cta_lo, cap, h0);
-        hd.P = P;
-        hd.s0 = (cta_lo < P && h0.req >= 0) ? h0.seg_start : -1;
-        hd.s1 = hd.s0 >= 0 ? h0.seg_start + h0.pages : -1;
-        hd.n = h0.n;
-        hd.g = h0.g;
+        if (any && !(warp == 0 && n_my > 0)) locate(p, lane, x, cap, h0);
+        if (any && h0.req >= 0) {
+            hs0 = h0.seg_start;
+            hs1 = h0.seg_start + h0.pages;
+            hn = h0.n;
+            hg = h0.g;
+        }
     }
     Cursor pc = cc;  // next page to issue (lane 0)
 
@@ -310,7 +318,21 @@ __global__ void __launch_bounds__(TcShape<D, BS>::NW * 32, 1)
     // stream: everything above only reads the (unchanging) metadata and the
     // cache. Queries, outputs and the workspace are touched after this wait.
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (warp == 0 && lane == 0) ws.hdr[blockIdx.x] = hd;
+    if (lane == 0 && warp <= 1) {
+        CtaHdr* hp = ws.hdr + blockIdx.x;
+        if (warp == 0) {
+            hp->P = P;
+            hp->a0 = hs0;
+            hp->a1 = hs1;
+            hp->an = hn;
+            hp->ag = hg;
+        } else {
+            hp->b0 = hs0;
+            hp->b1 = hs1;
+            hp->bn = hn;
+            hp->bg = hg;
+        }
+    }
 
     uint32_t qf[S::KD][NT][2];
     float o[S::KD][NT][4];
@@ -676,14 +698,19 @@ __global__ void __launch_bounds__(TcShape<D, BS>::NW * 32, 1)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Combines the CTA-level partials of every segment cut by a CTA boundary
-// (grid: one CTA per split-kernel CTA x query head of a group; D threads),
-// and zero-fills rows that have no key. Runs after attn_tc_persistent.
+// Finishes every segment cut by a CTA boundary from the CTA-level partials,
+// and zero-fills rows that have no key. Grid: one CTA per split-kernel CTA.
+// Each CTA spanned by a cut segment takes an equal share of that segment's
+// G x D outputs, so a long segment's merge spreads over all of its CTAs.
+// Pieces are combined in CTA order.
+constexpr int kMergeThreads = 256;
+
 template <int D, int NW>
-__global__ void __launch_bounds__(D) attn_tc_merge(const AttnParams p, int32_t ctas) {
-    __shared__ float sM, sL;
-    const int32_t c = blockIdx.x, h = blockIdx.y;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+__global__ void __launch_bounds__(kMergeThreads) attn_tc_merge(const AttnParams p, int32_t ctas) {
+    extern __shared__ float fac[];  // [pieces][G]: 2^(m - M) / L per CTA piece and head
+    __shared__ float red[kMergeThreads];
+    __shared__ float headM[16], headInvL[16];
+    const int32_t c = blockIdx.x;
     const int64_t cap64 = static_cast<int64_t>(p.max_blocks) * p.block_size;
     const int32_t cap = cap64 > 0x7fffffff ? 0x7fffffff : static_cast<int32_t>(cap64);
     __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out);
@@ -693,7 +720,7 @@ __global__ void __launch_bounds__(D) attn_tc_merge(const AttnParams p, int32_t c
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // rows with no key to attend: zero output, flag (rows spread over the CTAs)
-    if (h == 0 && p.num_reqs > 0) {
+    if (p.num_reqs > 0) {
         const int32_t rows = min(__ldg(p.cqsl + p.num_reqs), p.max_rows);
         for (int32_t n = c; n < rows; n += ctas) {
             int32_t req, kv;
@@ -708,81 +735,97 @@ __global__ void __launch_bounds__(D) attn_tc_merge(const AttnParams p, int32_t c
         }
     }
     if (launch_aborted(p)) return;
-    if (c == 0) return;  // CTA 0's start is never strictly inside a segment
 
     const TcWs ws = tc_ws(p, ctas, NW, D);
-    const CtaHdr H = ws.hdr[c];
-    if (H.s0 < 0) return;
-    const int64_t P = H.P, s0 = H.s0, s1 = H.s1;
-    const int32_t c_first = owner(s0, P, ctas);
-    if (c != c_first + 1) return;  // only the first CTA starting inside the segment merges
-    const int32_t c_last = owner(s1 - 1, P, ctas);
-    // A CTA keeps slot 0 for a segment that began before its slice and slot 1
-    // for one that begins inside it; only c_first holds the segment's start.
-    auto piece_of = [&](int32_t cc_) -> int64_t {
-        const int slot = cc_ == c_first ? 1 : 0;
-        return (static_cast<int64_t>(cc_) * 2 + slot) * p.G + h;
-    };
-    auto nonempty = [&](int32_t cc_) { return P * cc_ / ctas < P * (cc_ + 1) / ctas; };
-    // scale factor per CTA piece: 2^(m - M) / L (0 for an empty CTA or piece)
-    __shared__ float fac[kMaxMergePieces];
-    constexpr int NT4 = D;  // one thread per output element
-    __shared__ float red[NT4 / 32];
-    const int np = c_last - c_first + 1;
-    float mx = -INFINITY;
-    for (int i = threadIdx.x; i < np; i += NT4)
-        if (nonempty(c_first + i)) mx = fmaxf(mx, ws.c_ml[piece_of(c_first + i)].x);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    if (lane == 0) red[warp] = mx;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        float M = -INFINITY;
-        for (int w = 0; w < NT4 / 32; ++w) M = fmaxf(M, red[w]);
-        sM = M;
-    }
-    __syncthreads();
-    const float M = sM;
-    float lsum = 0.f;
-    for (int i = threadIdx.x; i < np; i += NT4) {
-        float f = 0.f;
-        if (nonempty(c_first + i)) {
-            const float2 ml = ws.c_ml[piece_of(c_first + i)];
-            if (ml.x != -INFINITY) f = exp2_approx(ml.x - M);
-            lsum += ml.y * f;
+    const CtaHdr Hc = ws.hdr[c];
+    const int64_t P = Hc.P;
+    if (P <= 0) return;
+    const int G = p.G;
+    for (int which = 0; which < 2; ++which) {
+        const int64_t s0 = which == 0 ? Hc.a0 : Hc.b0, s1 = which == 0 ? Hc.a1 : Hc.b1;
+        if (s0 < 0) continue;
+        if (which == 1 && s0 == Hc.a0) continue;  // same segment as the first
+        const int32_t c_first = owner(s0, P, ctas), c_last = owner(s1 - 1, P, ctas);
+        if (c_first == c_last) continue;  // not cut by a CTA boundary: finished in the split
+        // an empty CTA right before c_first starts at the same page and sees the
+        // same segment first, but holds none of it: only [c_first, c_last] share
+        if (c < c_first || c > c_last) continue;
+        const int np = c_last - c_first + 1;
+        const int k = c - c_first;        // this CTA's share of the outputs
+        const int32_t sn = which == 0 ? Hc.an : Hc.bn, sg = which == 0 ? Hc.ag : Hc.bg;
+        auto nonempty = [&](int32_t cc_) { return P * cc_ / ctas < P * (cc_ + 1) / ctas; };
+        // CTA c_first keeps slot 1 (the segment begins in its slice); the others slot 0
+        auto piece = [&](int i) -> int64_t {
+            return (static_cast<int64_t>(c_first + i) * 2 + (i == 0 ? 1 : 0)) * G;
+        };
+        // per-head max and sum over the pieces: thread t handles head t % 16
+        const int h16 = threadIdx.x & 15, sub = threadIdx.x >> 4;  // 16 x 16 threads
+        float mloc = -INFINITY;
+        if (h16 < G)
+            for (int i = sub; i < np; i += kMergeThreads / 16)
+                if (nonempty(c_first + i)) mloc = fmaxf(mloc, ws.c_ml[piece(i) + h16].x);
+        red[threadIdx.x] = mloc;
+        __syncthreads();
+        if (threadIdx.x < 16) {
+            float M = -INFINITY;
+            for (int j = 0; j < kMergeThreads / 16; ++j) M = fmaxf(M, red[j * 16 + threadIdx.x]);
+            headM[threadIdx.x] = M;
         }
-        fac[i] = f;
-    }
+        __syncthreads();
+        float lloc = 0.f;
+        if (h16 < G) {
+            const float M = headM[h16];
+            for (int i = sub; i < np; i += kMergeThreads / 16) {
+                float f = 0.f;
+                if (nonempty(c_first + i)) {
+                    const float2 ml = ws.c_ml[piece(i) + h16];
+                    if (ml.x != -INFINITY) f = exp2_approx(ml.x - M);
+                    lloc += ml.y * f;
+                }
+                fac[i * G + h16] = f;
+            }
+        }
+        red[threadIdx.x] = lloc;
+        __syncthreads();
+        if (threadIdx.x < 16) {
+            float L = 0.f;
+            for (int j = 0; j < kMergeThreads / 16; ++j) L += red[j * 16 + threadIdx.x];
+            headInvL[threadIdx.x] = 1.f / L;
+        }
+        __syncthreads();
+        // this CTA's share of the segment's G x D outputs
+        const int total = G * D;
+        const int per = (total + np - 1) / np;
+        const int lo = k * per, hi = min(total, lo + per);
+        const int64_t head0 = static_cast<int64_t>(sn) * p.H_q + sg * G;
+        const int64_t st = static_cast<int64_t>(2) * G * D;
+        for (int idx = lo + static_cast<int>(threadIdx.x); idx < hi; idx += kMergeThreads) {
+            const int h = idx / D;
+            const float* base = ws.c_o + piece(0) * D + idx;  // slot 1 of c_first
+            float acc = 0.f;
+            // an empty CTA's slot was never written (stale, maybe NaN): select, never scale by 0
+            const float f0 = fac[h];
+            acc += f0 != 0.f ? base[0] * f0 : 0.f;
+            const float* b1 = ws.c_o + (static_cast<int64_t>(c_first) * 2 * G) * D + idx;
+            int i = 1;
+            for (; i + 8 <= np; i += 8) {  // eight independent loads in flight
+                float a[8];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
-    __syncthreads();
-    if (lane == 0) red[warp] = lsum;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        float L = 0.f;
-        for (int w = 0; w < NT4 / 32; ++w) L += red[w];
-        sL = L;
-    }
-    __syncthreads();
-    const float invL = 1.f / sL;
-    const int d = threadIdx.x;
-    const float* base = ws.c_o + (static_cast<int64_t>(c_first) * 2 * p.G + h) * D + d;
-    // piece i lives at CTA c_first + i, slot 1 for i == 0 and 0 otherwise; an
-    // empty CTA's slot was never written (stale, maybe NaN): select, never scale by 0
-    auto term = [&](float a, float f) { return f != 0.f ? a * f : 0.f; };
-    const int64_t st = static_cast<int64_t>(2) * p.G * D;
-    float acc = term(base[static_cast<int64_t>(p.G) * D], fac[0]);
-    int i = 1;
-    for (; i + 8 <= np; i += 8) {  // eight independent loads in flight
-        float a[8];
+                for (int u = 0; u < 8; ++u) a[u] = b1[st * (i + u)];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) a[u] = base[st * (i + u)];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) acc += term(a[u], fac[i + u]);
+                for (int u = 0; u < 8; ++u) {
+                    const float f = fac[(i + u) * G + h];
+                    acc += f != 0.f ? a[u] * f : 0.f;
+                }
+            }
+            for (; i < np; ++i) {
+                const float f = fac[i * G + h];
+                acc += f != 0.f ? b1[st * i] * f : 0.f;
+            }
+            outp[head0 * D + idx] = __float2bfloat16_rn(acc * headInvL[h]);
+        }
+        __syncthreads();  // fac / head tables are rebuilt for the second segment
     }
-    for (; i < np; ++i) acc += term(base[st * i], fac[i]);
-    const int64_t head = static_cast<int64_t>(H.n) * p.H_q + H.g * p.G + h;
-    outp[head * D + d] = __float2bfloat16_rn(acc * invL);
 }
 
 // One-time (per device) setting of a kernel's dynamic shared memory limit.
@@ -827,9 +870,16 @@ cudaError_t launch_one(const CUtensorMap& mk, const CUtensorMap& mv, const AttnP
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, attn_tc_persistent<D, BS, NT>, mk, mv, q);
     if (e != cudaSuccess) return e;
-    cfg.gridDim = dim3(ctas, p.G);
-    cfg.blockDim = dim3(D);
-    cfg.dynamicSmemBytes = 0;
+    const int msmem = ctas * p.G * static_cast<int>(sizeof(float));  // factor table
+    const int msmem_max = ctas * 16 * static_cast<int>(sizeof(float));  // largest group
+    if (msmem_max > 48 * 1024) {  // only ever raise the limit above the default
+        static unsigned long long merge_smem_set = 0;
+        e = ensure_smem_attr(attn_tc_merge<D, S::NW>, msmem_max, merge_smem_set);
+        if (e != cudaSuccess) return e;
+    }
+    cfg.gridDim = dim3(ctas);
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.dynamicSmemBytes = msmem;
     return cudaLaunchKernelEx(&cfg, attn_tc_merge<D, S::NW>, q, static_cast<int32_t>(ctas));
 }
 

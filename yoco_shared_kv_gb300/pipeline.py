@@ -69,7 +69,9 @@ class DeviceStep:
             ws = N.yoco_cross_attn_workspace_size(max(self.rows_upper, 1), wl.num_q_heads,
                                                   wl.num_kv_heads, wl.head_dim, wl.block_size,
                                                   self.max_seq_len, torch_dtype(wl.dtype))
-            self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+            # all-ones bytes (NaN as fp32): the library must never read scratch it
+            # did not write in the same call, and this makes such a read visible
+            self.workspace = torch.full((max(ws, 16),), 255, dtype=torch.uint8, device=dev)
 
     def h2d(self, stream=None) -> int:
         """Re-copy the step's inputs from (pinned) host memory; returns bytes copied."""
