@@ -36,7 +36,7 @@ if ROOT not in sys.path:
 
 METRIC = "cross-decoder paged attn: KV GB/s (% of HBM peak), query rows/s at 1 GB300"
 FALLBACK_HBM_GBS = 6800.0
-DOMINANT_KERNEL = "attn_split_tc"
+DOMINANT_KERNEL = "attn_tc_persistent"
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.txt")
 
 
@@ -123,10 +123,16 @@ def measured_peaks() -> dict:
         return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
 
 
+KERNEL_SOURCES = ("attn_tc.cu", "attn_common.cuh", "common.cuh")
+
+
 def kernel_source_sha() -> str:
-    src = os.path.join(ROOT, "yoco_shared_kv_gb300", "csrc", "cross_attn.cu")
-    with open(src, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Hash of the sources the dominant kernel is built from."""
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "yoco_shared_kv_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def profiled_traffic(workload: str):

@@ -701,15 +701,19 @@ __global__ void __launch_bounds__(TcShape<D, BS>::NW * 32, 1)
 // Finishes every segment cut by a CTA boundary from the CTA-level partials,
 // and zero-fills rows that have no key. Grid: one CTA per split-kernel CTA.
 // Each CTA spanned by a cut segment takes an equal share of that segment's
-// G x D outputs, so a long segment's merge spreads over all of its CTAs.
-// Pieces are combined in CTA order.
+// G x D outputs, so a long segment's merge spreads over all of its CTAs. A
+// CTA shares at most two segments (those of its first and last page); the
+// two halves of the CTA work on them at the same time. Pieces are combined
+// in CTA order.
 constexpr int kMergeThreads = 256;
+constexpr int kMergeHalf = kMergeThreads / 2;
+constexpr int kMergeRegPieces = 8;  // per-thread piece statistics kept in registers
 
 template <int D, int NW>
 __global__ void __launch_bounds__(kMergeThreads) attn_tc_merge(const AttnParams p, int32_t ctas) {
-    extern __shared__ float fac[];  // [pieces][G]: 2^(m - M) / L per CTA piece and head
+    extern __shared__ float fac[];  // [2][pieces][G]: 2^(m - M) per CTA piece and head
     __shared__ float red[kMergeThreads];
-    __shared__ float headM[16], headInvL[16];
+    __shared__ float headM[2][16], headInvL[2][16];
     const int32_t c = blockIdx.x;
     const int64_t cap64 = static_cast<int64_t>(p.max_blocks) * p.block_size;
     const int32_t cap = cap64 > 0x7fffffff ? 0x7fffffff : static_cast<int32_t>(cap64);
@@ -718,13 +722,15 @@ __global__ void __launch_bounds__(kMergeThreads) attn_tc_merge(const AttnParams 
     // and let the next kernel (the next layer's split) start its prologue
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const TcWs ws = tc_ws(p, ctas, NW, D);
+    const CtaHdr Hc = ws.hdr[c];
 
-    // rows with no key to attend: zero output, flag (rows spread over the CTAs)
-    if (p.num_reqs > 0) {
-        const int32_t rows = min(__ldg(p.cqsl + p.num_reqs), p.max_rows);
-        for (int32_t n = c; n < rows; n += ctas) {
-            int32_t req, kv;
-            if (!locate_row(p.cqsl, p.num_reqs, n, p.seq_lens, req, kv)) break;
+    // rows with no key to attend: zero output, flag (requests spread over the CTAs)
+    for (int32_t r = c; r < p.num_reqs; r += ctas) {
+        const int32_t c0 = __ldg(p.cqsl + r), c1 = __ldg(p.cqsl + r + 1);
+        const int32_t seq = __ldg(p.seq_lens + r), k = c1 - c0;
+        for (int32_t n = c0; n < c1 && n < p.max_rows; ++n) {
+            const int32_t kv = seq - k + (n - c0) + 1;
             if (kv <= 0) {
                 for (int i = threadIdx.x; i < p.H_q * D; i += blockDim.x)
                     outp[static_cast<int64_t>(n) * p.H_q * D + i] = __float2bfloat16_rn(0.f);
@@ -735,96 +741,123 @@ __global__ void __launch_bounds__(kMergeThreads) attn_tc_merge(const AttnParams 
         }
     }
     if (launch_aborted(p)) return;
-
-    const TcWs ws = tc_ws(p, ctas, NW, D);
-    const CtaHdr Hc = ws.hdr[c];
     const int64_t P = Hc.P;
     if (P <= 0) return;
     const int G = p.G;
+
+    // the (at most two) cut segments this CTA shares
+    int64_t seg0[2];
+    int32_t segn[2], segg[2], cf[2], np_[2];
+    int nseg = 0;
     for (int which = 0; which < 2; ++which) {
         const int64_t s0 = which == 0 ? Hc.a0 : Hc.b0, s1 = which == 0 ? Hc.a1 : Hc.b1;
-        if (s0 < 0) continue;
-        if (which == 1 && s0 == Hc.a0) continue;  // same segment as the first
+        if (s0 < 0 || (which == 1 && s0 == Hc.a0)) continue;
         const int32_t c_first = owner(s0, P, ctas), c_last = owner(s1 - 1, P, ctas);
-        if (c_first == c_last) continue;  // not cut by a CTA boundary: finished in the split
-        // an empty CTA right before c_first starts at the same page and sees the
-        // same segment first, but holds none of it: only [c_first, c_last] share
-        if (c < c_first || c > c_last) continue;
-        const int np = c_last - c_first + 1;
-        const int k = c - c_first;        // this CTA's share of the outputs
-        const int32_t sn = which == 0 ? Hc.an : Hc.bn, sg = which == 0 ? Hc.ag : Hc.bg;
-        auto nonempty = [&](int32_t cc_) { return P * cc_ / ctas < P * (cc_ + 1) / ctas; };
-        // CTA c_first keeps slot 1 (the segment begins in its slice); the others slot 0
-        auto piece = [&](int i) -> int64_t {
-            return (static_cast<int64_t>(c_first + i) * 2 + (i == 0 ? 1 : 0)) * G;
-        };
-        // per-head max and sum over the pieces: thread t handles head t % 16
-        const int h16 = threadIdx.x & 15, sub = threadIdx.x >> 4;  // 16 x 16 threads
-        float mloc = -INFINITY;
-        if (h16 < G)
-            for (int i = sub; i < np; i += kMergeThreads / 16)
-                if (nonempty(c_first + i)) mloc = fmaxf(mloc, ws.c_ml[piece(i) + h16].x);
-        red[threadIdx.x] = mloc;
-        __syncthreads();
-        if (threadIdx.x < 16) {
-            float M = -INFINITY;
-            for (int j = 0; j < kMergeThreads / 16; ++j) M = fmaxf(M, red[j * 16 + threadIdx.x]);
-            headM[threadIdx.x] = M;
-        }
-        __syncthreads();
-        float lloc = 0.f;
-        if (h16 < G) {
-            const float M = headM[h16];
-            for (int i = sub; i < np; i += kMergeThreads / 16) {
-                float f = 0.f;
-                if (nonempty(c_first + i)) {
-                    const float2 ml = ws.c_ml[piece(i) + h16];
-                    if (ml.x != -INFINITY) f = exp2_approx(ml.x - M);
-                    lloc += ml.y * f;
-                }
-                fac[i * G + h16] = f;
-            }
-        }
-        red[threadIdx.x] = lloc;
-        __syncthreads();
-        if (threadIdx.x < 16) {
-            float L = 0.f;
-            for (int j = 0; j < kMergeThreads / 16; ++j) L += red[j * 16 + threadIdx.x];
-            headInvL[threadIdx.x] = 1.f / L;
-        }
-        __syncthreads();
-        // this CTA's share of the segment's G x D outputs
-        const int total = G * D;
-        const int per = (total + np - 1) / np;
-        const int lo = k * per, hi = min(total, lo + per);
-        const int64_t head0 = static_cast<int64_t>(sn) * p.H_q + sg * G;
-        const int64_t st = static_cast<int64_t>(2) * G * D;
-        for (int idx = lo + static_cast<int>(threadIdx.x); idx < hi; idx += kMergeThreads) {
-            const int h = idx / D;
-            const float* base = ws.c_o + piece(0) * D + idx;  // slot 1 of c_first
-            float acc = 0.f;
-            // an empty CTA's slot was never written (stale, maybe NaN): select, never scale by 0
-            const float f0 = fac[h];
-            acc += f0 != 0.f ? base[0] * f0 : 0.f;
-            const float* b1 = ws.c_o + (static_cast<int64_t>(c_first) * 2 * G) * D + idx;
-            int i = 1;
-            for (; i + 8 <= np; i += 8) {  // eight independent loads in flight
-                float a[8];
+        // not cut (finished in the split kernel), or this CTA holds none of it
+        // (an empty CTA right before c_first starts at the segment's first page)
+        if (c_first == c_last || c < c_first || c > c_last) continue;
+        seg0[nseg] = s0;
+        segn[nseg] = which == 0 ? Hc.an : Hc.bn;
+        segg[nseg] = which == 0 ? Hc.ag : Hc.bg;
+        cf[nseg] = c_first;
+        np_[nseg] = c_last - c_first + 1;
+        ++nseg;
+    }
+    if (nseg == 0) return;
+    (void)seg0;
+    // threads [0, half) take segment 0, [half, 2 half) segment 1 (all of them
+    // take segment 0 when there is only one)
+    const int half = nseg == 2 ? kMergeHalf : kMergeThreads;
+    const int si = nseg == 2 ? static_cast<int>(threadIdx.x) / kMergeHalf : 0;
+    const int tl = static_cast<int>(threadIdx.x) - si * half;  // thread index within the half
+    const int32_t c_first = cf[si], np = np_[si];
+    const int k = c - c_first;  // this CTA's share of the outputs
+    auto nonempty = [&](int32_t cc_) { return P * cc_ / ctas < P * (cc_ + 1) / ctas; };
+    // CTA c_first keeps slot 1 (the segment begins in its slice); the others slot 0
+    auto piece = [&](int i) -> int64_t {
+        return (static_cast<int64_t>(c_first + i) * 2 + (i == 0 ? 1 : 0)) * G;
+    };
+    float* ftab = fac + si * ctas * G;
+    // per-head max and sum over the pieces: thread tl handles head tl % 16
+    const int h16 = tl & 15, sub = tl >> 4, nsub = half >> 4;
+    float2 mlr[kMergeRegPieces];
+    float mloc = -INFINITY;
 #pragma unroll
-                for (int u = 0; u < 8; ++u) a[u] = b1[st * (i + u)];
+    for (int j = 0; j < kMergeRegPieces; ++j) {
+        const int i = sub + j * nsub;
+        mlr[j] = make_float2(-INFINITY, 0.f);
+        if (h16 < G && i < np && nonempty(c_first + i)) mlr[j] = ws.c_ml[piece(i) + h16];
+        mloc = fmaxf(mloc, mlr[j].x);
+    }
+    for (int i = sub + kMergeRegPieces * nsub; h16 < G && i < np; i += nsub)  // rare: long spans
+        if (nonempty(c_first + i)) mloc = fmaxf(mloc, ws.c_ml[piece(i) + h16].x);
+    red[threadIdx.x] = mloc;
+    __syncthreads();
+    if (tl < 16) {
+        float M = -INFINITY;
+        for (int j = 0; j < nsub; ++j) M = fmaxf(M, red[si * half + j * 16 + tl]);
+        headM[si][tl] = M;
+    }
+    __syncthreads();
+    float lloc = 0.f;
+    if (h16 < G) {
+        const float M = headM[si][h16];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const float f = fac[(i + u) * G + h];
-                    acc += f != 0.f ? a[u] * f : 0.f;
-                }
+        for (int j = 0; j < kMergeRegPieces; ++j) {
+            const int i = sub + j * nsub;
+            if (i < np) {
+                const float f = mlr[j].x != -INFINITY ? exp2_approx(mlr[j].x - M) : 0.f;
+                lloc += mlr[j].y * f;
+                ftab[i * G + h16] = f;
             }
-            for (; i < np; ++i) {
-                const float f = fac[i * G + h];
-                acc += f != 0.f ? b1[st * i] * f : 0.f;
-            }
-            outp[head0 * D + idx] = __float2bfloat16_rn(acc * headInvL[h]);
         }
-        __syncthreads();  // fac / head tables are rebuilt for the second segment
+        for (int i = sub + kMergeRegPieces * nsub; i < np; i += nsub) {
+            float f = 0.f;
+            if (nonempty(c_first + i)) {
+                const float2 ml = ws.c_ml[piece(i) + h16];
+                if (ml.x != -INFINITY) f = exp2_approx(ml.x - M);
+                lloc += ml.y * f;
+            }
+            ftab[i * G + h16] = f;
+        }
+    }
+    red[threadIdx.x] = lloc;
+    __syncthreads();
+    if (tl < 16) {
+        float L = 0.f;
+        for (int j = 0; j < nsub; ++j) L += red[si * half + j * 16 + tl];
+        headInvL[si][tl] = 1.f / L;
+    }
+    __syncthreads();
+    // this CTA's share of the segment's G x D outputs
+    const int total = G * D;
+    const int per = (total + np - 1) / np;
+    const int lo = k * per, hi = min(total, lo + per);
+    const int64_t head0 = static_cast<int64_t>(segn[si]) * p.H_q + segg[si] * G;
+    const int64_t st = static_cast<int64_t>(2) * G * D;
+    for (int idx = lo + tl; idx < hi; idx += half) {
+        const int h = idx / D;
+        // an empty CTA's slot was never written (stale, maybe NaN): select, never scale by 0
+        const float f0 = ftab[h];
+        const float v0 = ws.c_o[piece(0) * D + idx];  // slot 1 of c_first
+        float acc = f0 != 0.f ? v0 * f0 : 0.f;
+        const float* b1 = ws.c_o + (static_cast<int64_t>(c_first) * 2 * G) * D + idx;
+        int i = 1;
+        for (; i + 8 <= np; i += 8) {  // eight independent loads in flight
+            float a[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) a[u] = b1[st * (i + u)];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const float f = ftab[(i + u) * G + h];
+                acc += f != 0.f ? a[u] * f : 0.f;
+            }
+        }
+        for (; i < np; ++i) {
+            const float f = ftab[i * G + h];
+            acc += f != 0.f ? b1[st * i] * f : 0.f;
+        }
+        outp[head0 * D + idx] = __float2bfloat16_rn(acc * headInvL[si][h]);
     }
 }
 
@@ -870,8 +903,8 @@ cudaError_t launch_one(const CUtensorMap& mk, const CUtensorMap& mv, const AttnP
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, attn_tc_persistent<D, BS, NT>, mk, mv, q);
     if (e != cudaSuccess) return e;
-    const int msmem = ctas * p.G * static_cast<int>(sizeof(float));  // factor table
-    const int msmem_max = ctas * 16 * static_cast<int>(sizeof(float));  // largest group
+    const int msmem = 2 * ctas * p.G * static_cast<int>(sizeof(float));  // factor tables
+    const int msmem_max = 2 * ctas * 16 * static_cast<int>(sizeof(float));  // largest group
     if (msmem_max > 48 * 1024) {  // only ever raise the limit above the default
         static unsigned long long merge_smem_set = 0;
         e = ensure_smem_attr(attn_tc_merge<D, S::NW>, msmem_max, merge_smem_set);
