@@ -143,10 +143,10 @@ def profiled_traffic(workload: str):
     except OSError:
         return None
     kv = dict(l.split("=", 1) for l in lines if "=" in l and not l.startswith("#"))
-    if kv.get("source_sha") != kernel_source_sha() or kv.get("workload") != workload:
+    if kv.get("source_sha") != kernel_source_sha():
         return None
     try:
-        return float(kv["dram_bytes_per_launch"])
+        return float(kv[workload])
     except (KeyError, ValueError):
         return None
 
@@ -203,6 +203,23 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
         return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def aggregate_ranks(elapsed_ms: float, kv_bytes: float, rows: float, world: int, device):
+    """Whole-job numbers: the slowest rank's time, the units of every rank.
+
+    Replicas share nothing on the data path; this is the only collective.
+    """
+    if world <= 1:
+        return float(elapsed_ms), float(kv_bytes), float(rows)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([elapsed_ms, float(kv_bytes), float(rows)], dtype=torch.float64,
+                     device=device)
+    tmax = t.clone()
+    dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(tmax[0]), float(t[1]), float(t[2])
 
 
 # --------------------------------------------------------------- our arm
@@ -288,18 +305,8 @@ def run_ours(args, rank, world, local):
     stream.synchronize()
     attn_launch_ms = a0.elapsed_time(a1) / (reps * L)
 
-    max_ms = elapsed_ms
-    total_kv_bytes = acc["kv_bytes_step"] * args.steps
-    total_rows = acc["rows"] * L * args.steps
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([elapsed_ms, float(total_kv_bytes), float(total_rows)], dtype=torch.float64,
-                         device=dev)
-        tmax = t.clone()
-        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
-        dist.all_reduce(t, op=dist.ReduceOp.SUM)
-        max_ms = float(tmax[0])
-        total_kv_bytes, total_rows = float(t[1]), float(t[2])
+    max_ms, total_kv_bytes, total_rows = aggregate_ranks(
+        elapsed_ms, acc["kv_bytes_step"] * args.steps, acc["rows"] * L * args.steps, world, dev)
     clocks = sampler.stop() if sampler else None
     if dw.error_bits() != 0:
         raise RuntimeError(f"device error bits {dw.error_bits():#x}")
