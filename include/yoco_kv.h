@@ -69,6 +69,9 @@ typedef enum {
 
 typedef enum { YOCO_F32 = 0, YOCO_BF16 = 1 } yoco_dtype_t;
 
+/* Flags of yoco_cross_attn_paged. */
+#define YOCO_ATTN_REVERSE 0x1u /* bf16 path: walk each worker's pages last to first (see below) */
+
 /* Bits OR-ed into *err_word by device code. */
 #define YOCO_DEVERR_PAGE_RANGE 0x1   /* block_table entry outside [0, num_blocks) */
 #define YOCO_DEVERR_POS_RANGE 0x2    /* position beyond max_blocks_per_req * block_size, or negative */
@@ -153,6 +156,11 @@ size_t yoco_cross_attn_workspace_size(int32_t max_rows, int32_t num_q_heads, int
  *   max_rows               host bound on the number of rows (grid size)
  *   max_seq_len            host bound on seq_lens (sizes the split-KV grid)
  *   scale                  softmax scale (1/sqrt(head_dim) for the pages' definition)
+ *   flags                  0 or YOCO_ATTN_REVERSE. The serial layers re-read one cache
+ *                          ("YOCO 论文与推理数据流详解" §11); with the flag set on every other
+ *                          layer, a layer starts on the pages the previous one read last,
+ *                          which are still in L2. The result is the same up to summation order.
+ *                          Ignored on the fp32 path; other bits are rejected.
  *   workspace              device scratch of >= yoco_cross_attn_workspace_size(...) bytes,
  *                          16-byte aligned; contents need no initialisation
  *   err_word               device int32 or NULL
@@ -168,8 +176,8 @@ yoco_status_t yoco_cross_attn_paged(const void* q, const void* k_cache, const vo
                                     int32_t max_rows, int32_t max_seq_len, int32_t num_q_heads,
                                     int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                                     int32_t num_blocks, float scale, yoco_dtype_t dtype,
-                                    void* workspace, size_t workspace_bytes, int32_t* err_word,
-                                    void* stream);
+                                    uint32_t flags, void* workspace, size_t workspace_bytes,
+                                    int32_t* err_word, void* stream);
 
 /*
  * yoco_cross_attn_paged_noalloc — yoco_cross_attn_paged for callers that

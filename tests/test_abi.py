@@ -59,21 +59,22 @@ def test_host_validation_rejects_before_launch(lib_path):
     L.yoco_cross_attn_paged.restype = ctypes.c_int
     vp, i32 = ctypes.c_void_p, ctypes.c_int32
     L.yoco_cross_attn_paged.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32,
-                                        i32, i32, i32, ctypes.c_float, ctypes.c_int, vp,
-                                        ctypes.c_size_t, vp, vp]
+                                        i32, i32, i32, ctypes.c_float, ctypes.c_int,
+                                        ctypes.c_uint32, vp, ctypes.c_size_t, vp, vp]
     args = dict(hq=8, hkv=2, d=256, bs=16, dt=1)
 
     def call(**kw):
         a = {**args, **kw}
         return L.yoco_cross_attn_paged(None, None, None, None, None, 4, None, None, 1, 1, 64,
                                        a["hq"], a["hkv"], a["d"], a["bs"], 100, 0.0625, a["dt"],
-                                       None, 0, None, None)
+                                       a.get("flags", 0), None, 0, None, None)
     assert call(d=96) == 2          # unsupported head_dim
     assert call(bs=8) == 2          # unsupported block size
     assert call(hq=7) == 1          # H_q not a multiple of H_kv
     assert call(hq=34, hkv=2) == 2  # group of 17
     assert call(dt=5) == 2          # unknown dtype
     assert call() == 1              # null pointers
+    assert call(flags=0x4) == 1     # unknown flag bit
     L.yoco_select_cross_rows.restype = ctypes.c_int
     L.yoco_select_cross_rows.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp]
     assert L.yoco_select_cross_rows(None, None, -1, None, None, None, None, None) == 1

@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_PKG, "libyoco_kv.so")
 
 YOCO_OK, YOCO_ERR_INVALID_ARG, YOCO_ERR_UNSUPPORTED, YOCO_ERR_WORKSPACE, YOCO_ERR_CUDA = range(5)
 YOCO_F32, YOCO_BF16 = 0, 1
+YOCO_ATTN_REVERSE = 0x1
 DEVERR_PAGE_RANGE = 0x1
 DEVERR_POS_RANGE = 0x2
 DEVERR_EMPTY_ROW = 0x4
@@ -55,7 +56,8 @@ def _load() -> ctypes.CDLL:
     L.yoco_cross_attn_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.c_int]
     L.yoco_cross_attn_paged.restype = ctypes.c_int
     L.yoco_cross_attn_paged.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32,
-                                        i32, i32, i32, ctypes.c_float, ctypes.c_int, vp, sz, vp, vp]
+                                        i32, i32, i32, ctypes.c_float, ctypes.c_int,
+                                        ctypes.c_uint32, vp, sz, vp, vp]
     L.yoco_set_l2_window.restype = ctypes.c_int
     L.yoco_set_l2_window.argtypes = [vp, vp, sz, ctypes.c_float]
     L.yoco_status_string.restype = ctypes.c_char_p
@@ -162,7 +164,7 @@ def yoco_cross_attn_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch
                           out: torch.Tensor, block_table: torch.Tensor, seq_lens: torch.Tensor,
                           cross_query_start_loc: torch.Tensor, max_seq_len: int, scale: float,
                           workspace: Optional[torch.Tensor], err_word: Optional[torch.Tensor] = None,
-                          stream=None, max_rows: Optional[int] = None) -> None:
+                          stream=None, max_rows: Optional[int] = None, flags: int = 0) -> None:
     """One layer: ``q/out [max_rows, H_q, D]`` against pools ``[num_blocks, H_kv, bs, D]``."""
     num_blocks, H_kv, bs, D = k_cache.shape
     rows_cap, H_q, Dq = q.shape
@@ -175,8 +177,8 @@ def yoco_cross_attn_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _i32(block_table, "block_table"),
         block_table.shape[1], _i32(seq_lens, "seq_lens"),
         _i32(cross_query_start_loc, "cross_query_start_loc"), R, max_rows, int(max_seq_len), H_q,
-        H_kv, D, bs, num_blocks, float(scale), dtype_code(q.dtype), _ptr(workspace), ws_bytes,
-        None if err_word is None else _i32(err_word, "err_word"), _stream(stream)))
+        H_kv, D, bs, num_blocks, float(scale), dtype_code(q.dtype), int(flags), _ptr(workspace),
+        ws_bytes, None if err_word is None else _i32(err_word, "err_word"), _stream(stream)))
 
 
 def yoco_cross_attn_paged_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,

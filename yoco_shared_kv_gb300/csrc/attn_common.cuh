@@ -24,6 +24,7 @@ struct AttnParams {
     int32_t split_pages;        // CUDA-core path: logical pages per split
     int32_t max_splits;         // CUDA-core path
     float scale_log2;           // softmax scale * log2(e)
+    int32_t reverse;            // tensor-core path: walk each worker's pages from the end
 };
 
 // Wait limit for one asynchronous page copy before a kernel gives up.

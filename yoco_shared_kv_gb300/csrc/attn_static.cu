@@ -70,6 +70,6 @@ extern "C" yoco_status_t yoco_cross_attn_paged_noalloc(
     return yoco_cross_attn_paged(q, k_cache, v_cache, out, block_table, max_blocks_per_req,
                                  seq_lens, cross_query_start_loc, num_reqs, max_rows,
                                  max_seq_len, num_q_heads, num_kv_heads, head_dim, block_size,
-                                 num_blocks, scale, dtype, scratch, kStaticScratchBytes, err_word,
-                                 stream);
+                                 num_blocks, scale, dtype, 0u, scratch, kStaticScratchBytes,
+                                 err_word, stream);
 }

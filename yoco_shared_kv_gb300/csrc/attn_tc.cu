@@ -171,6 +171,31 @@ __device__ __forceinline__ void advance(const AttnParams& p, Cursor& c, int32_t 
     }
 }
 
+// Previous page in the flattened order (skips rows without keys).
+__device__ __forceinline__ void retreat(const AttnParams& p, Cursor& c, int32_t cap) {
+    if (--c.pp >= 0) return;
+    if (--c.g >= 0) {  // same row, previous kv head
+        c.pp = c.pages - 1;
+        c.seg_start -= c.pages;
+        return;
+    }
+    for (;;) {
+        if (--c.n < 0) return;
+        while (c.req > 0 && __ldg(p.cqsl + c.req) > c.n) --c.req;
+        const int32_t c0 = __ldg(p.cqsl + c.req), c1 = __ldg(p.cqsl + c.req + 1);
+        const int32_t kv = __ldg(p.seq_lens + c.req) - (c1 - c0) + (c.n - c0) + 1;
+        const int32_t pg = row_pages(kv, cap, p.block_size);
+        if (pg > 0) {
+            c.pages = pg;
+            c.kv_len = min(kv, cap);
+            c.g = p.H_kv - 1;
+            c.pp = pg - 1;
+            c.seg_start -= pg;
+            return;
+        }
+    }
+}
+
 // Index of the worker (of `workers` equal slices of P) owning flattened page x.
 __device__ __forceinline__ int32_t owner(int64_t x, int64_t P, int32_t workers) {
     return static_cast<int32_t>(((x + 1) * workers - 1) / P);
@@ -223,7 +248,7 @@ __device__ __forceinline__ TcWs tc_ws(const AttnParams& p, int ctas, int nw, int
 
 // --------------------------------------------------------------- kernel
 
-template <int D, int BS, int NT>
+template <int D, int BS, int NT, bool REV>
 __global__ void __launch_bounds__(TcShape<D, BS>::NW * 32, 1)
     attn_tc_persistent(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
@@ -267,9 +292,16 @@ __global__ void __launch_bounds__(TcShape<D, BS>::NW * 32, 1)
 
     uint8_t* wbuf = smem + warp * STAGES * S::STAGE_BYTES;
     uint64_t* wbar = bars + warp * STAGES;
+    // Odd layers may walk each slice backwards (REV): a layer then starts on
+    // the pages the previous layer read last, which are still in L2.
+    constexpr bool rev = REV;
+    auto step = [&](Cursor& c) {
+        if (rev) retreat(p, c, cap);
+        else advance(p, c, cap);
+    };
     Cursor cc;  // page being consumed
     cc.req = -1;
-    if (n_my > 0) locate(p, lane, my_lo, cap, cc);
+    if (n_my > 0) locate(p, lane, rev ? my_hi - 1 : my_lo, cap, cc);
     // header for the merge kernel: warp 0 finds the segment of page cta_lo,
     // warp 1 the segment of page cta_hi - 1
     int64_t hs0 = -1, hs1 = -1;
@@ -278,7 +310,7 @@ __global__ void __launch_bounds__(TcShape<D, BS>::NW * 32, 1)
         const int64_t x = warp == 0 ? cta_lo : cta_hi - 1;
         const bool any = warp == 0 ? cta_lo < P : cta_hi > cta_lo;
         Cursor h0 = cc;
-        if (any && !(warp == 0 && n_my > 0)) locate(p, lane, x, cap, h0);
+        if (any && !(warp == 0 && n_my > 0 && !rev)) locate(p, lane, x, cap, h0);
         if (any && h0.req >= 0) {
             hs0 = h0.seg_start;
             hs1 = h0.seg_start + h0.pages;
@@ -308,7 +340,7 @@ __global__ void __launch_bounds__(TcShape<D, BS>::NW * 32, 1)
                 tma_load_2d(vd + c * S::SUB_BYTES, &tm_v, c * 64, y, bar);
             }
         }
-        advance(p, pc, cap);
+        step(pc);
     };
     if (lane == 0) {
         const int pro = n_my < STAGES ? n_my : STAGES;
@@ -369,13 +401,13 @@ __global__ void __launch_bounds__(TcShape<D, BS>::NW * 32, 1)
     reset_state();
     const float sl2 = p.scale_log2;
     bool aborted = false;
-    bool reload_first = false;  // this warp's first-segment piece sits in global memory
+    int reload_slot = -1;  // slot of this warp's piece flushed mid-stream (to global memory)
     int consumed = 0;
     // one piece: [G][D] o, then [G] (m, l); 16-byte stride keeps float4 access aligned
     const int piece_bytes = (p.G * (D * 4 + 8) + 15) & ~15;
 
     for (int i = 0; i < n_my; ++i) {
-        if (i == 0 || cc.pp == 0) load_q(cc.n, cc.g);
+        if (i == 0 || cc.pp == (rev ? cc.pages - 1 : 0)) load_q(cc.n, cc.g);
         const int st = i % STAGES;
         if (!mbar_wait_bounded(wbar + st, (i / STAGES) & 1, kWaitLimitNs)) {
             aborted = true;
@@ -509,7 +541,7 @@ __global__ void __launch_bounds__(TcShape<D, BS>::NW * 32, 1)
         __syncwarp();
         if (lane == 0 && i + STAGES < n_my) issue(i + STAGES);
 
-        if (cc.pp == cc.pages - 1 || i == n_my - 1) {  // segment (or slice) ends here
+        if (cc.pp == (rev ? 0 : cc.pages - 1) || i == n_my - 1) {  // segment or slice done
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -540,7 +572,7 @@ __global__ void __launch_bounds__(TcShape<D, BS>::NW * 32, 1)
                 const int slot = s0 < my_lo ? 0 : 1;
                 // A piece flushed at the end of the slice goes to this warp's
                 // ring, idle from here on; the one flushed mid-stream (the
-                // warp's first segment) goes to global memory and is brought
+                // first segment walked) goes to global memory and is brought
                 // back into the ring after streaming.
                 const bool at_end = (i == n_my - 1);
                 float* dst_o;
@@ -552,7 +584,7 @@ __global__ void __launch_bounds__(TcShape<D, BS>::NW * 32, 1)
                     const int64_t piece = (static_cast<int64_t>(wid) * 2 + slot) * p.G;
                     dst_o = ws.w_o + piece * D;
                     dst_ml = ws.w_ml + piece;
-                    reload_first = true;
+                    reload_slot = slot;
                 }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
@@ -578,7 +610,7 @@ __global__ void __launch_bounds__(TcShape<D, BS>::NW * 32, 1)
             }
             reset_state();
         }
-        advance(p, cc, cap);
+        step(cc);
     }
 
     if (aborted) {
@@ -591,11 +623,11 @@ __global__ void __launch_bounds__(TcShape<D, BS>::NW * 32, 1)
             atomicExch(&abort_flag, 1);
         }
     }
-    if (reload_first && !aborted) {
-        // bring the mid-stream piece (slot 0) back next to the slice-end one
-        const int64_t piece = static_cast<int64_t>(wid) * 2 * p.G;
+    if (reload_slot >= 0 && !aborted) {
+        // bring the mid-stream piece back next to the slice-end one
+        const int64_t piece = (static_cast<int64_t>(wid) * 2 + reload_slot) * p.G;
         const float4* src = reinterpret_cast<const float4*>(ws.w_o + piece * D);
-        float4* dst = reinterpret_cast<float4*>(wbuf);
+        float4* dst = reinterpret_cast<float4*>(wbuf + reload_slot * piece_bytes);
         const int nv = p.G * D / 4;
         for (int v0 = lane; v0 < nv; v0 += 32 * 8) {  // 8 loads in flight per lane
             float4 r[8];
@@ -606,7 +638,8 @@ __global__ void __launch_bounds__(TcShape<D, BS>::NW * 32, 1)
             for (int u = 0; u < 8; ++u)
                 if (v0 + u * 32 < nv) dst[v0 + u * 32] = r[u];
         }
-        float2* dml = reinterpret_cast<float2*>(reinterpret_cast<float*>(wbuf) + p.G * D);
+        float2* dml = reinterpret_cast<float2*>(
+            reinterpret_cast<float*>(wbuf + reload_slot * piece_bytes) + p.G * D);
         for (int h = lane; h < p.G; h += 32) dml[h] = ws.w_ml[piece + h];
     }
     __syncthreads();  // pieces are in the warps' rings, headers in shared memory
@@ -880,8 +913,10 @@ template <int D, int BS, int NT>
 cudaError_t launch_one(const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p, int sms,
                        cudaStream_t s) {
     using S = TcShape<D, BS>;
-    static unsigned long long smem_set = 0;  // one flag word per kernel instantiation
-    cudaError_t e = ensure_smem_attr(attn_tc_persistent<D, BS, NT>, S::SMEM, smem_set);
+    static unsigned long long smem_fwd = 0, smem_rev = 0;  // one flag word per kernel
+    auto kernel = p.reverse ? attn_tc_persistent<D, BS, NT, true>
+                            : attn_tc_persistent<D, BS, NT, false>;
+    cudaError_t e = ensure_smem_attr(kernel, S::SMEM, p.reverse ? smem_rev : smem_fwd);
     if (e != cudaSuccess) return e;
     const int ctas = tc_ctas(sms);
     AttnParams q = p;  // workspace: outputs of all pieces, then their (m, l), then headers
@@ -901,7 +936,7 @@ cudaError_t launch_one(const CUtensorMap& mk, const CUtensorMap& mv, const AttnP
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, attn_tc_persistent<D, BS, NT>, mk, mv, q);
+    e = cudaLaunchKernelEx(&cfg, kernel, mk, mv, q);
     if (e != cudaSuccess) return e;
     const int msmem = 2 * ctas * p.G * static_cast<int>(sizeof(float));  // factor tables
     const int msmem_max = 2 * ctas * 16 * static_cast<int>(sizeof(float));  // largest group

@@ -157,8 +157,10 @@ extern "C" yoco_status_t yoco_cross_attn_paged(
     int32_t max_blocks_per_req, const int32_t* seq_lens, const int32_t* cross_query_start_loc,
     int32_t num_reqs, int32_t max_rows, int32_t max_seq_len, int32_t num_q_heads,
     int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale,
-    yoco_dtype_t dtype, void* workspace, size_t workspace_bytes, int32_t* err_word, void* stream) {
+    yoco_dtype_t dtype, uint32_t flags, void* workspace, size_t workspace_bytes, int32_t* err_word,
+    void* stream) {
     using namespace yoco;
+    if (flags & ~static_cast<uint32_t>(YOCO_ATTN_REVERSE)) return YOCO_ERR_INVALID_ARG;
     if (!dtype_ok(dtype) || !head_dim_ok(head_dim) || !block_size_ok(block_size))
         return YOCO_ERR_UNSUPPORTED;
     if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0)
@@ -201,6 +203,7 @@ extern "C" yoco_status_t yoco_cross_attn_paged(
     p.split_pages = pl.split_pages;
     p.max_splits = pl.max_splits;
     p.scale_log2 = scale * kLog2e;
+    p.reverse = (flags & YOCO_ATTN_REVERSE) ? 1 : 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (pl.tc) {

@@ -83,7 +83,8 @@ class DeviceStep:
 
 
 class DeviceWorkload:
-    def __init__(self, wl, device="cuda", pin_host: bool = False, sentinel: bool = True):
+    def __init__(self, wl, device="cuda", pin_host: bool = False, sentinel: bool = True,
+                 alternate="auto"):
         self.wl = wl
         self.device = torch.device(device)
         tdt = torch_dtype(wl.dtype)
@@ -98,6 +99,13 @@ class DeviceWorkload:
             self.k_cache = torch.empty(shape, dtype=tdt, device=self.device)
             self.v_cache = torch.empty(shape, dtype=tdt, device=self.device)
         self.err = torch.zeros(1, dtype=torch.int32, device=self.device)
+        if alternate == "auto":
+            # Reverse every other layer's page walk only when the cache does not
+            # fit in L2; a cache that fits is served from L2 in any order.
+            pool_bytes = 2 * self.k_cache.numel() * self.k_cache.element_size()
+            l2 = torch.cuda.get_device_properties(self.device).L2_cache_size
+            alternate = pool_bytes > l2
+        self.alternate = bool(alternate)
         self.fill = DeviceStep(wl, wl.fill, device, pin_host) if wl.fill is not None else None
         self.steps: List[DeviceStep] = [DeviceStep(wl, s, device, pin_host) for s in wl.steps]
 
@@ -115,11 +123,14 @@ class DeviceWorkload:
 
     def attend(self, ds: DeviceStep, layer: int, stream=None, q: Optional[torch.Tensor] = None,
                out: Optional[torch.Tensor] = None) -> None:
+        """One cross-decoder layer. Odd layers walk the pages last to first, so each
+        layer starts on what the previous one left in L2 (when `alternate` is on)."""
         d = ds.dev
+        flags = N.YOCO_ATTN_REVERSE if (self.alternate and layer % 2 == 1) else 0
         N.yoco_cross_attn_paged(d["q"][layer] if q is None else q, self.k_cache, self.v_cache,
                                 ds.out[layer] if out is None else out, d["block_table"],
                                 d["seq_lens"], ds.cqsl, ds.max_seq_len, self.wl.scale,
-                                ds.workspace, self.err, stream)
+                                ds.workspace, self.err, stream, flags=flags)
 
     def run_fill(self, stream=None) -> None:
         if self.fill is not None:
