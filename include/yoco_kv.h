@@ -226,6 +226,17 @@ size_t yoco_cross_attn_noalloc_capacity(void);
  */
 yoco_status_t yoco_set_l2_window(void* stream, void* base, size_t bytes, float hit_ratio);
 
+/*
+ * yoco_selftest_wait_timeout — diagnostic for the bounded waits. The pages
+ * have no counterpart. Launches one CTA that waits, with the library's
+ * bounded-wait helper and a limit of limit_us microseconds (1..2000000), on
+ * an asynchronous-copy barrier that nothing completes; the wait gives up,
+ * the CTA sets YOCO_DEVERR_TIMEOUT in *err_word (device int32, required)
+ * and returns, leaving the context usable. Used by the tests to show that a
+ * copy that never lands ends in a status, not a hang.
+ */
+yoco_status_t yoco_selftest_wait_timeout(int32_t* err_word, uint32_t limit_us, void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* yoco_status_string(yoco_status_t status);
 

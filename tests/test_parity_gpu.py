@@ -307,3 +307,20 @@ def test_attention_writes_only_its_outputs(P, N, lens, H_q, H_kv, D, bs):
     got = gpu_out(out)[None]
     assert np.isfinite(got).all()
     assert np.abs(got - ref).max() <= ATOL["bf16"]
+
+
+def test_bounded_wait_gives_up_with_a_status(P, N):
+    """A copy that never lands ends in YOCO_DEVERR_TIMEOUT, and the context stays usable."""
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    N.yoco_selftest_wait_timeout(err, 20000)  # 20 ms limit
+    torch.cuda.synchronize()
+    assert int(err.item()) & N.DEVERR_TIMEOUT
+    # the same process keeps working: a normal step still matches the oracle
+    wl = SMALL[1]()
+    dw = P.DeviceWorkload(wl)
+    dw.run_all()
+    torch.cuda.synchronize()
+    assert dw.error_bits() == 0
+    got = gpu_out(dw.steps[0].out)
+    ref = oracle_step_out(wl, wl.steps[0])
+    assert np.abs(got - ref).max() <= ATOL["bf16"]

@@ -29,7 +29,8 @@ DEVERR_TIMEOUT = 0x10
 EXPORTED = ("yoco_kv_append", "yoco_select_cross_rows", "yoco_cross_attn_workspace_size",
             "yoco_cross_attn_paged", "yoco_set_l2_window", "yoco_status_string", "yoco_version",
             "yoco_last_cuda_error", "yoco_last_cuda_error_string",
-            "yoco_cross_attn_paged_noalloc", "yoco_cross_attn_noalloc_capacity")
+            "yoco_cross_attn_paged_noalloc", "yoco_cross_attn_noalloc_capacity",
+            "yoco_selftest_wait_timeout")
 
 
 class YocoError(RuntimeError):
@@ -74,6 +75,8 @@ def _load() -> ctypes.CDLL:
                                                 ctypes.c_int, vp, vp]
     L.yoco_cross_attn_noalloc_capacity.restype = sz
     L.yoco_cross_attn_noalloc_capacity.argtypes = []
+    L.yoco_selftest_wait_timeout.restype = ctypes.c_int
+    L.yoco_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint32, vp]
     return L
 
 
@@ -204,6 +207,12 @@ def yoco_cross_attn_paged_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cach
 
 def yoco_cross_attn_noalloc_capacity() -> int:
     return int(lib.yoco_cross_attn_noalloc_capacity())
+
+
+def yoco_selftest_wait_timeout(err_word: torch.Tensor, limit_us: int = 20000, stream=None) -> None:
+    """Diagnostic: a bounded wait on a barrier nothing completes must end in TIMEOUT."""
+    _check("yoco_selftest_wait_timeout", lib.yoco_selftest_wait_timeout(
+        _i32(err_word, "err_word"), int(limit_us), _stream(stream)))
 
 
 def yoco_set_l2_window(base: Optional[torch.Tensor], nbytes: int, hit_ratio: float = 1.0,

@@ -65,3 +65,26 @@ extern "C" yoco_status_t yoco_set_l2_window(void* stream, void* base, size_t byt
     YOCO_CUDA_OK(cudaStreamSetAttribute(s, cudaStreamAttributeAccessPolicyWindow, &attr));
     return YOCO_OK;
 }
+
+namespace yoco {
+namespace {
+// One thread arms a barrier for bytes that no copy will deliver and waits on
+// it with the same bounded helper the attention kernel uses.
+__global__ void selftest_wait_kernel(int32_t* err, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&bar, 1024);  // no copy is issued: the phase never completes
+    if (!mbar_wait_bounded(&bar, 0, limit_ns)) set_err(err, YOCO_DEVERR_TIMEOUT);
+}
+}  // namespace
+}  // namespace yoco
+
+extern "C" yoco_status_t yoco_selftest_wait_timeout(int32_t* err_word, uint32_t limit_us,
+                                                    void* stream) {
+    if (err_word == nullptr || limit_us == 0 || limit_us > 2000000u) return YOCO_ERR_INVALID_ARG;
+    yoco::selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        err_word, static_cast<uint64_t>(limit_us) * 1000ull);
+    return yoco::cuda_status(cudaGetLastError());
+}
