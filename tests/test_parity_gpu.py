@@ -324,3 +324,26 @@ def test_bounded_wait_gives_up_with_a_status(P, N):
     got = gpu_out(dw.steps[0].out)
     ref = oracle_step_out(wl, wl.steps[0])
     assert np.abs(got - ref).max() <= ATOL["bf16"]
+
+
+def test_chunked_prefill_and_speculative_rows(P):
+    """Three steps: a prompt prefilled in chunks (no cross row until the last chunk),
+    a decode, and a 3-token speculative verify asking for all trailing rows."""
+    from workloads import chunked_prefill_spec
+    wl = chunked_prefill_spec()
+    dw = P.DeviceWorkload(wl)
+    dw.run_fill()
+    for i, step in enumerate(wl.steps):
+        dw.run_step(i)
+        torch.cuda.synchronize()
+        assert dw.error_bits() == 0
+        ds = dw.steps[i]
+        o_rows, o_cq, n = oracle.select_cross_rows(step.query_start_loc, step.rows_per_req)
+        assert int(ds.num_rows.item()) == n == step.rows_upper
+        assert np.array_equal(ds.row_indices.cpu().numpy()[:n], o_rows)
+        assert np.array_equal(ds.cqsl.cpu().numpy(), o_cq)
+        got = gpu_out(ds.out)
+        ref = oracle_step_out(wl, step)
+        assert np.abs(got - ref).max() <= ATOL["bf16"], i
+    kp, vp = oracle_pools(wl)
+    assert np.array_equal(pool_bits(dw.k_cache), oracle_bits(kp))

@@ -356,6 +356,41 @@ def shared_prefix(seed: int = 1004, num_reqs: int = 256, prefix_len: int = 4096,
                  description=f"shared prefix {prefix_len} + tails U[{tail_lo},{tail_hi}] x {num_reqs}")
 
 
+def chunked_prefill_spec(seed: int = 1005, H_q: int = 8, H_kv: int = 2, D: int = 128, bs: int = 16,
+                         layers: int = 3, dtype: str = "bf16") -> Workload:
+    """Three scheduling steps mixing a chunked prefill, a decode and a speculative decode.
+
+    Request A: a 100-token prompt prefilled in chunks of 40, 40 and 20; only the
+    last chunk's last token enters the cross-decoder (rows_per_req 0, 0, 1: the
+    vLLM post notes that intermediate chunks could be skipped). Request B
+    decodes one token per step after a 300-token context. Request C verifies 3
+    draft tokens per step after a 200-token context and asks for all 3 trailing
+    rows (the metadata builder's example gives a request several rows).
+    """
+    rng_struct = np.random.default_rng([seed, 0])
+    rng_kv = np.random.default_rng([seed, 1])
+    rng_q = np.random.default_rng([seed, 2])
+    full = [100, 303, 209]
+    blocks = [-(-n // bs) for n in full]
+    num_blocks, pages = _allocate_pages(rng_struct, blocks, 1.2)
+    private_k = [_normal(rng_kv, (n, H_kv, D), dtype) for n in full]
+    private_v = [_normal(rng_kv, (n, H_kv, D), dtype) for n in full]
+    wl = Workload(name=f"chunked_prefill_spec_{dtype}", dtype=dtype, num_q_heads=H_q,
+                  num_kv_heads=H_kv, head_dim=D, block_size=bs, num_blocks=num_blocks,
+                  layers=layers, scale=1.0 / np.sqrt(D), max_blocks_per_req=max(blocks),
+                  req_pages=pages, prefix_len=0, prefix_k=None, prefix_v=None,
+                  private_k=private_k, private_v=private_v, fill=None, steps=[],
+                  description="chunked prefill (40/40/20) + decode + 3-token speculative decode")
+    schedule = [
+        ([(0, 40, 40), (1, 301, 1), (2, 203, 3)], [0, 1, 3]),
+        ([(0, 80, 40), (1, 302, 1), (2, 206, 3)], [0, 1, 3]),
+        ([(0, 100, 20), (1, 303, 1), (2, 209, 3)], [1, 1, 3]),
+    ]
+    wl.fill = _assemble_step(wl, [(1, 300, 300), (2, 200, 200)], None, None, with_q=False)
+    wl.steps = [_assemble_step(wl, e, rpr, rng_q, with_q=True) for e, rpr in schedule]
+    return wl
+
+
 # The five workloads at full size, indexed as they are listed in the
 # problem statement (0 = toy ... 4 = shared prefix).
 FULL = {
