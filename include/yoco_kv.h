@@ -227,6 +227,27 @@ size_t yoco_cross_attn_noalloc_capacity(void);
 yoco_status_t yoco_set_l2_window(void* stream, void* base, size_t bytes, float hit_ratio);
 
 /*
+ * yoco_cross_decoder_bytes — predicted HBM bytes of one scheduling step's
+ * cross-decoder attention, for a traffic-aware scheduler. "YOCO 论文与推理数据流
+ * 详解" §11 and §18.2: the global K^/V^ is written once but re-read by every
+ * cross-decoder layer, so a request's decode traffic grows with its context
+ * length times the number of cross-decoder layers. Per request r with k_r
+ * cross rows (the yoco_select_cross_rows rule) and row i's key count kv_i:
+ *   layers * sum_i ( kv_i * 2 * H_kv * head_dim * elem      K^ and V^
+ *                  + 2 * H_q * head_dim * elem               query and output
+ *                  + 4 * ceil(kv_i / block_size) * H_kv )    block-table entries
+ * with elem = 2 (bf16) or 4 (fp32) and kv_i clamped at 0.
+ *   query_start_loc, seq_lens   host int32 [num_reqs + 1] / [num_reqs]
+ *   rows_per_req                host int32 [num_reqs] or NULL (= 1)
+ *   per_req_bytes               host int64 out [num_reqs] or NULL
+ * Returns the total, or -1 for invalid arguments. Pure host arithmetic.
+ */
+int64_t yoco_cross_decoder_bytes(const int32_t* query_start_loc, const int32_t* rows_per_req,
+                                 const int32_t* seq_lens, int32_t num_reqs, int32_t layers,
+                                 int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                 int32_t block_size, yoco_dtype_t dtype, int64_t* per_req_bytes);
+
+/*
  * yoco_selftest_wait_timeout — diagnostic for the bounded waits. The pages
  * have no counterpart. Launches one CTA that waits, with the library's
  * bounded-wait helper and a limit of limit_us microseconds (1..2000000), on

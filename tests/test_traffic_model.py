@@ -1,0 +1,65 @@
+"""The traffic model (host C function) against the benchmark's accounting and
+against DRAM bytes ncu measured for the attention kernel."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from tests.conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def N():
+    from yoco_shared_kv_gb300 import build
+    build.build()
+    from yoco_shared_kv_gb300 import _native
+    return _native
+
+
+def _model(N, wl, st):
+    from yoco_shared_kv_gb300.pipeline import torch_dtype
+    return N.yoco_cross_decoder_bytes(st.query_start_loc, st.rows_per_req, st.seq_lens, wl.layers,
+                                      wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.block_size,
+                                      torch_dtype(wl.dtype))
+
+
+@pytest.mark.parametrize("idx", [0, 1, 2, 3, 4])
+def test_model_equals_bench_accounting(N, idx):
+    import bench
+    from workloads import SMALL
+    wl = SMALL[idx]()
+    for st in wl.steps:
+        tot, per = _model(N, wl, st)
+        assert tot == bench.accounting(wl, st)["attn_bytes_layer"] * wl.layers
+        assert per.sum() == tot
+
+
+def test_model_counts_rows_like_selection(N):
+    from workloads import chunked_prefill_spec
+    wl = chunked_prefill_spec()
+    st = wl.steps[0]  # A: non-final chunk -> no row, so no bytes
+    tot, per = _model(N, wl, st)
+    assert per[0] == 0 and per[1] > 0 and per[2] > per[1]
+    # three speculative rows see 201, 202, 203 keys
+    D, H_kv, H_q, bs, L = wl.head_dim, wl.num_kv_heads, wl.num_q_heads, wl.block_size, wl.layers
+    exp = sum(kv * 2 * H_kv * D * 2 + 2 * H_q * D * 2 + 4 * -(-kv // bs) * H_kv
+              for kv in (201, 202, 203)) * L
+    assert per[2] == exp
+
+
+def test_model_predicts_measured_dram_bytes(N):
+    """profiles/traffic.txt holds ncu DRAM bytes per attention launch at full size."""
+    import bench
+    lines = open(os.path.join(ROOT, "profiles", "traffic.txt")).read().splitlines()
+    meas = dict(l.split("=", 1) for l in lines if "=" in l and not l.startswith("#"))
+    for cfg, name in ((1, "pure_decode_bf16"), (3, "long_context_bf16")):
+        wl = bench.make_workload(cfg)
+        tot, _ = _model(N, wl, wl.steps[-1])
+        per_layer = tot / wl.layers
+        assert abs(float(meas[name]) / per_layer - 1.0) < 0.005  # within 0.5 %
+
+
+def test_model_rejects_bad_arguments(N):
+    with pytest.raises(ValueError):
+        N.yoco_cross_decoder_bytes([0, 3, 2], None, [5, 5], 1, 8, 2, 128, 16, torch.bfloat16)

@@ -30,7 +30,7 @@ EXPORTED = ("yoco_kv_append", "yoco_select_cross_rows", "yoco_cross_attn_workspa
             "yoco_cross_attn_paged", "yoco_set_l2_window", "yoco_status_string", "yoco_version",
             "yoco_last_cuda_error", "yoco_last_cuda_error_string",
             "yoco_cross_attn_paged_noalloc", "yoco_cross_attn_noalloc_capacity",
-            "yoco_selftest_wait_timeout")
+            "yoco_selftest_wait_timeout", "yoco_cross_decoder_bytes")
 
 
 class YocoError(RuntimeError):
@@ -77,6 +77,9 @@ def _load() -> ctypes.CDLL:
     L.yoco_cross_attn_noalloc_capacity.argtypes = []
     L.yoco_selftest_wait_timeout.restype = ctypes.c_int
     L.yoco_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint32, vp]
+    L.yoco_cross_decoder_bytes.restype = ctypes.c_int64
+    L.yoco_cross_decoder_bytes.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, ctypes.c_int,
+                                           vp]
     return L
 
 
@@ -207,6 +210,24 @@ def yoco_cross_attn_paged_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cach
 
 def yoco_cross_attn_noalloc_capacity() -> int:
     return int(lib.yoco_cross_attn_noalloc_capacity())
+
+
+def yoco_cross_decoder_bytes(query_start_loc, rows_per_req, seq_lens, layers: int,
+                             num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
+                             dtype: torch.dtype):
+    """Traffic model on host arrays: (total bytes, per-request bytes)."""
+    import numpy as np
+    qsl = np.ascontiguousarray(query_start_loc, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    rpr = None if rows_per_req is None else np.ascontiguousarray(rows_per_req, dtype=np.int32)
+    R = qsl.shape[0] - 1
+    per = np.zeros(max(R, 1), dtype=np.int64)
+    tot = lib.yoco_cross_decoder_bytes(
+        qsl.ctypes.data, None if rpr is None else rpr.ctypes.data, sl.ctypes.data, R, layers,
+        num_q_heads, num_kv_heads, head_dim, block_size, dtype_code(dtype), per.ctypes.data)
+    if tot < 0:
+        raise ValueError("invalid arguments")
+    return int(tot), per[:R]
 
 
 def yoco_selftest_wait_timeout(err_word: torch.Tensor, limit_us: int = 20000, stream=None) -> None:

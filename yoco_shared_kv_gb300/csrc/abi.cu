@@ -88,3 +88,35 @@ extern "C" yoco_status_t yoco_selftest_wait_timeout(int32_t* err_word, uint32_t 
         err_word, static_cast<uint64_t>(limit_us) * 1000ull);
     return yoco::cuda_status(cudaGetLastError());
 }
+
+// Traffic model: the algorithmic bytes one cross-decoder step moves per request.
+extern "C" int64_t yoco_cross_decoder_bytes(const int32_t* query_start_loc,
+                                            const int32_t* rows_per_req, const int32_t* seq_lens,
+                                            int32_t num_reqs, int32_t layers, int32_t num_q_heads,
+                                            int32_t num_kv_heads, int32_t head_dim,
+                                            int32_t block_size, yoco_dtype_t dtype,
+                                            int64_t* per_req_bytes) {
+    if (num_reqs < 0 || layers < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        block_size <= 0 || !yoco::dtype_ok(dtype))
+        return -1;
+    if (num_reqs > 0 && (query_start_loc == nullptr || seq_lens == nullptr)) return -1;
+    const int64_t elem = static_cast<int64_t>(yoco::elem_size(dtype));
+    int64_t total = 0;
+    for (int32_t r = 0; r < num_reqs; ++r) {
+        const int64_t q_len = static_cast<int64_t>(query_start_loc[r + 1]) - query_start_loc[r];
+        const int64_t want = rows_per_req ? rows_per_req[r] : 1;
+        if (q_len < 0 || want < 0) return -1;
+        const int64_t k = want < q_len ? want : q_len;
+        int64_t b = 0;
+        for (int64_t i = 0; i < k; ++i) {
+            int64_t kv = static_cast<int64_t>(seq_lens[r]) - k + i + 1;
+            if (kv < 0) kv = 0;
+            b += kv * 2 * num_kv_heads * head_dim * elem + 2ll * num_q_heads * head_dim * elem +
+                 4 * ((kv + block_size - 1) / block_size) * num_kv_heads;
+        }
+        b *= layers;
+        if (per_req_bytes) per_req_bytes[r] = b;
+        total += b;
+    }
+    return total;
+}
