@@ -45,6 +45,19 @@ def lib():
                                         ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                         ctypes.c_double, _f64p, ctypes.POINTER(ctypes.c_int64),
                                         ctypes.c_int32]
+        L.oracle_e4m3_encode_array.restype = None
+        L.oracle_e4m3_encode_array.argtypes = [ctypes.c_void_p, ctypes.c_int64, _u8p]
+        L.oracle_e4m3_decode_array.restype = None
+        L.oracle_e4m3_decode_array.argtypes = [_u8p, ctypes.c_int64, _f64p]
+        L.oracle_kv_append_e4m3.restype = ctypes.c_int64
+        L.oracle_kv_append_e4m3.argtypes = [ctypes.c_void_p, ctypes.c_void_p, _u8p, _u8p,
+                                            ctypes.c_void_p, _i32p, ctypes.c_int32, _i32p, _i32p,
+                                            ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                            ctypes.c_int32, ctypes.c_int32]
+        L.oracle_e4m3_gather.restype = ctypes.c_int32
+        L.oracle_e4m3_gather.argtypes = [_u8p, ctypes.c_void_p, ctypes.c_int32, _i32p,
+                                         ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                         ctypes.c_int32, ctypes.c_int32, _f64p]
         _lib = L
     return _lib
 
@@ -148,3 +161,61 @@ def cross_attn(q: np.ndarray, K_req: Sequence[np.ndarray], V_req: Sequence[np.nd
                                  _p(out, _f64p), cap.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
                                  max(1, int(nthreads)))
     return out, int(st)
+
+
+# ------------------------------------------------------------------ e4m3 cache
+
+def e4m3_encode(x) -> np.ndarray:
+    """float32 values -> e4m3 codes (nearest, ties to even, saturating at +-448)."""
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    out = np.zeros(x.shape, dtype=np.uint8)
+    lib().oracle_e4m3_encode_array(x.ctypes.data, x.size, _p(out, _u8p))
+    return out
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """e4m3 codes -> float64 values (NaN for the two NaN codes)."""
+    c = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+    out = np.zeros(c.shape, dtype=np.float64)
+    lib().oracle_e4m3_decode_array(_p(c, _u8p), c.size, _p(out, _f64p))
+    return out
+
+
+def kv_append_e4m3(k_new: np.ndarray, v_new: np.ndarray, k_pool: np.ndarray, v_pool: np.ndarray,
+                   scales: np.ndarray, block_table, seq_lens, query_start_loc,
+                   block_size: int) -> int:
+    """Quantising append: bf16 bits [T, H_kv, D] into uint8 pools [num_blocks, H_kv, bs, D];
+    scales float32 [num_blocks, H_kv, 4] = (k_scale, v_scale, -, -). Returns skipped count."""
+    assert k_pool.dtype == np.uint8 and v_pool.dtype == np.uint8
+    assert k_pool.flags.c_contiguous and v_pool.flags.c_contiguous
+    num_blocks, H_kv, bs, D = k_pool.shape
+    assert bs == block_size
+    sc = np.ascontiguousarray(scales, dtype=np.float32)
+    assert sc.shape == (num_blocks, H_kv, 4)
+    kn = np.ascontiguousarray(k_new).view(np.uint16)
+    vn = np.ascontiguousarray(v_new).view(np.uint16)
+    bt = _i32(block_table)
+    if bt.ndim == 1:
+        bt = bt.reshape(1, -1)
+    qsl, sl = _i32(query_start_loc), _i32(seq_lens)
+    R = qsl.shape[0] - 1
+    max_blocks = bt.shape[1] if bt.size else 1
+    return int(lib().oracle_kv_append_e4m3(kn.ctypes.data, vn.ctypes.data, _p(k_pool, _u8p),
+                                           _p(v_pool, _u8p), sc.ctypes.data, _p(bt, _i32p),
+                                           max_blocks, _p(sl, _i32p), _p(qsl, _i32p), R,
+                                           num_blocks, bs, H_kv, D))
+
+
+def e4m3_gather(pool: np.ndarray, scales: np.ndarray, which: int, bt_row,
+                n_tokens: int) -> np.ndarray:
+    """Dequantised [n_tokens, H_kv, D] float64 of one request (which: 0 = K scale, 1 = V)."""
+    num_blocks, H_kv, bs, D = pool.shape
+    sc = np.ascontiguousarray(scales, dtype=np.float32)
+    bt = _i32(bt_row)
+    out = np.zeros((max(n_tokens, 0), H_kv, D), dtype=np.float64)
+    st = lib().oracle_e4m3_gather(_p(np.ascontiguousarray(pool), _u8p), sc.ctypes.data, which,
+                                  _p(bt, _i32p), n_tokens, num_blocks, bs, H_kv, D,
+                                  _p(out, _f64p))
+    if st != 0:
+        raise ValueError("page index out of range")
+    return out

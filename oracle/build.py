@@ -19,8 +19,8 @@ def build(force: bool = False) -> str:
         return LIB
     tmp = LIB + f".tmp{os.getpid()}"
     # No fast-math: the oracle keeps IEEE double semantics.
-    cmd = ["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-pthread", "-Wall", "-Wextra",
-           "-o", tmp, SRC, "-lm"]
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-shared", "-fPIC", "-pthread", "-Wall",
+           "-Wextra", "-o", tmp, SRC, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, LIB)
     return LIB

@@ -29,8 +29,13 @@
  *               rows of a request with seq_len tokens sees
  *               seq_len - k_r + i + 1 keys.
  *
- * Arithmetic is float64 throughout; bf16 inputs arrive already widened
- * exactly to double by the caller.
+ *   e4m3      — "KV cache memory systems", "Quantized cache changes attention
+ *               inputs": the cache may hold 8-bit values plus per-page,
+ *               per-head K and V scales (see the e4m3 section below).
+ *
+ * Arithmetic is float64 throughout, except where a float32 division decides
+ * an 8-bit code; bf16 inputs arrive already widened exactly to double by the
+ * caller.
  */
 #include <math.h>
 #include <pthread.h>
@@ -110,6 +115,156 @@ int64_t oracle_kv_append(const uint8_t* k_new, const uint8_t* v_new, uint8_t* k_
         }
     }
     return skipped;
+}
+
+/* -------------------------------------------------------------- e4m3 cache */
+
+/*
+ * "KV cache memory systems", "Quantized cache changes attention inputs": a
+ * quantized cache stores fewer bytes per scalar and adds scale metadata;
+ * keys and values may need separate calibration, per head. Readings: the
+ * 8-bit format is e4m3 (sign bit, 4 exponent bits with bias 7, 3 mantissa
+ * bits, subnormals, no infinities, S.1111.111 = NaN, largest finite 448);
+ * each (physical page, kv head) has one scale for K and one for V, given by
+ * the caller as a record of four floats {k_scale, v_scale, unused, unused};
+ * code c stands for decode(c) * scale, and a value x is stored as
+ * encode(x / scale), the division in float32, rounded to the nearest code
+ * with ties to the even code, saturating at +-448.
+ */
+double oracle_e4m3_decode(uint8_t c)
+{
+    int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);        /* (m / 8) * 2^-6 */
+    else
+        v = ldexp(8.0 + m, e - 10);      /* (1 + m / 8) * 2^(e - 7) */
+    return sign ? -v : v;
+}
+
+uint8_t oracle_e4m3_encode(float x)
+{
+    if (isnan(x))
+        return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a >= 448.0)
+        return sign | 0x7E;
+    int code;
+    if (a < ldexp(1.0, -6)) {
+        /* subnormal spacing 2^-9; a result of 8 is the smallest normal */
+        code = (int)nearbyint(ldexp(a, 9));
+    } else {
+        int e2;
+        frexp(a, &e2);                   /* a in [2^(e2-1), 2^e2) */
+        int e = e2 - 1;
+        int M = (int)nearbyint(ldexp(a, 3 - e));  /* 8..16; 16 carries into the exponent */
+        code = ((e + 7) << 3) + (M - 8);
+    }
+    if (code > 0x7E)
+        code = 0x7E;
+    return sign | (uint8_t)code;
+}
+
+void oracle_e4m3_encode_array(const float* x, int64_t n, uint8_t* out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_e4m3_encode(x[i]);
+}
+
+void oracle_e4m3_decode_array(const uint8_t* c, int64_t n, double* out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_e4m3_decode(c[i]);
+}
+
+static float bf16_bits_to_float(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/*
+ * Append with quantisation: k_new/v_new are bf16 bits [T][H_kv][D]; pools
+ * hold one e4m3 byte per element, [num_blocks][H_kv][block_size][D];
+ * scales is [num_blocks][H_kv][4] floats. Placement is the one of
+ * oracle_kv_append. A (token, head) whose scale is not a positive finite
+ * number is skipped; skipped (token, head) pairs are counted and returned.
+ */
+int64_t oracle_kv_append_e4m3(const uint16_t* k_new, const uint16_t* v_new, uint8_t* k_pool,
+                              uint8_t* v_pool, const float* scales, const int32_t* block_table,
+                              int32_t max_blocks, const int32_t* seq_lens, const int32_t* qsl,
+                              int32_t num_reqs, int32_t num_blocks, int32_t block_size,
+                              int32_t num_kv_heads, int32_t head_dim)
+{
+    int64_t skipped = 0;
+    for (int32_t r = 0; r < num_reqs; ++r) {
+        int64_t q_len = (int64_t)qsl[r + 1] - (int64_t)qsl[r];
+        for (int64_t j = 0; j < q_len; ++j) {
+            int64_t tok = (int64_t)qsl[r] + j;
+            int64_t pos = (int64_t)seq_lens[r] - q_len + j;
+            if (pos < 0 || pos / block_size >= max_blocks) {
+                skipped += num_kv_heads;
+                continue;
+            }
+            int64_t page = block_table[(int64_t)r * max_blocks + pos / block_size];
+            int64_t slot = pos % block_size;
+            if (page < 0 || page >= num_blocks) {
+                skipped += num_kv_heads;
+                continue;
+            }
+            for (int32_t h = 0; h < num_kv_heads; ++h) {
+                const float ks = scales[(page * num_kv_heads + h) * 4 + 0];
+                const float vs = scales[(page * num_kv_heads + h) * 4 + 1];
+                if (!(ks > 0.0f) || !(vs > 0.0f) || isinf(ks) || isinf(vs)) {
+                    ++skipped;
+                    continue;
+                }
+                size_t dst = (size_t)((page * num_kv_heads + h) * block_size + slot) * head_dim;
+                size_t src = (size_t)(tok * num_kv_heads + h) * head_dim;
+                for (int32_t d = 0; d < head_dim; ++d) {
+                    const float kq = bf16_bits_to_float(k_new[src + d]) / ks;
+                    const float vq = bf16_bits_to_float(v_new[src + d]) / vs;
+                    k_pool[dst + d] = oracle_e4m3_encode(kq);
+                    v_pool[dst + d] = oracle_e4m3_encode(vq);
+                }
+            }
+        }
+    }
+    return skipped;
+}
+
+/*
+ * The first n_tokens positions of one request read back through its block
+ * table row and dequantised: out[pos][h][d] = decode(code) * scale, with
+ * scale = scales[page][h][which] (which = 0 for K, 1 for V). Returns 0, or
+ * -1 if a page index is out of range (those entries are left untouched).
+ */
+int32_t oracle_e4m3_gather(const uint8_t* pool, const float* scales, int32_t which,
+                           const int32_t* bt_row, int64_t n_tokens, int32_t num_blocks,
+                           int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                           double* out)
+{
+    int32_t st = 0;
+    for (int64_t pos = 0; pos < n_tokens; ++pos) {
+        int64_t page = bt_row[pos / block_size], slot = pos % block_size;
+        if (page < 0 || page >= num_blocks) {
+            st = -1;
+            continue;
+        }
+        for (int32_t h = 0; h < num_kv_heads; ++h) {
+            const double sc = (double)scales[(page * num_kv_heads + h) * 4 + which];
+            const uint8_t* src = pool + ((page * num_kv_heads + h) * block_size + slot) * head_dim;
+            double* dst = out + (pos * num_kv_heads + h) * head_dim;
+            for (int32_t d = 0; d < head_dim; ++d)
+                dst[d] = oracle_e4m3_decode(src[d]) * sc;
+        }
+    }
+    return st;
 }
 
 /* --------------------------------------------------------------- attention */

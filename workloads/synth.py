@@ -27,6 +27,7 @@ pattern so that both consumers read the very same bits.
 from __future__ import annotations
 
 import dataclasses
+import zlib
 from typing import List, Optional, Sequence, Tuple
 
 import numpy as np
@@ -412,6 +413,22 @@ SMALL = {
     3: lambda: long_context(2003, num_reqs=2, ctx=3000, layers=3),
     4: lambda: shared_prefix(2004, num_reqs=5, prefix_len=256, tail_lo=1, tail_hi=70, layers=3),
 }
+
+
+def page_scales(wl: Workload, lo: float = 3.5, hi: float = 5.0) -> np.ndarray:
+    """Scale records of an 8-bit (e4m3) cache: float32 ``[num_blocks, H_kv, 4]``
+    holding (k_scale, v_scale, 0, 0) per physical page and kv head.
+
+    Recipe: each scale is A / 448 with A ~ U[lo, hi), i.e. the page-head can
+    hold values up to A before saturating; K and V draw independently. For the
+    N(0,1) values of these workloads that saturates a few values in 10^4 to
+    10^6. Seeded by the workload's name and pool size.
+    """
+    rng = np.random.default_rng([zlib.crc32(wl.name.encode()), wl.num_blocks, 4])
+    rec = np.zeros((wl.num_blocks, wl.num_kv_heads, 4), dtype=np.float32)
+    rec[..., 0] = (rng.uniform(lo, hi, size=rec.shape[:2]) / 448.0).astype(np.float32)
+    rec[..., 1] = (rng.uniform(lo, hi, size=rec.shape[:2]) / 448.0).astype(np.float32)
+    return rec
 
 
 def describe(wl: Workload) -> dict:
