@@ -55,6 +55,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--seed-offset", type=int, default=0)
+    ap.add_argument("--kv", choices=["native", "e4m3"], default="native",
+                    help="cache format: the workload's dtype, or e4m3 with per-page scales")
     return ap.parse_args(argv)
 
 
@@ -93,16 +95,22 @@ def cross_rows_kv_lens(step) -> np.ndarray:
     return np.asarray(lens, dtype=np.int64)
 
 
-def accounting(wl, step) -> dict:
-    """Algorithmic bytes of one step (per layer and per step)."""
+def accounting(wl, step, e4m3: bool = False) -> dict:
+    """Algorithmic bytes of one step (per layer and per step). With an e4m3 cache
+    the keys/values take one byte each and every page read adds its 16-byte
+    scale record; queries and outputs stay in the workload's dtype."""
     from workloads import elem_bytes
     sz = elem_bytes(wl.dtype)
+    kv_sz = 1 if e4m3 else sz
     kv = cross_rows_kv_lens(step)
     rows = int(kv.shape[0])
-    kv_bytes_layer = int(kv.sum()) * 2 * wl.num_kv_heads * wl.head_dim * sz
+    kv_bytes_layer = int(kv.sum()) * 2 * wl.num_kv_heads * wl.head_dim * kv_sz
     qo_bytes_layer = 2 * rows * wl.num_q_heads * wl.head_dim * sz
-    bt_bytes_layer = 4 * int(np.sum((kv + wl.block_size - 1) // wl.block_size)) * wl.num_kv_heads
-    append_bytes = 2 * 2 * step.num_tokens * wl.num_kv_heads * wl.head_dim * sz  # read + write
+    page_meta = 4 + (16 if e4m3 else 0)
+    bt_bytes_layer = page_meta * int(np.sum((kv + wl.block_size - 1) // wl.block_size)) * \
+        wl.num_kv_heads
+    # read + write
+    append_bytes = 2 * step.num_tokens * wl.num_kv_heads * wl.head_dim * (sz + kv_sz)
     return {
         "rows": rows,
         "kv_bytes_layer": kv_bytes_layer,
@@ -123,7 +131,7 @@ def measured_peaks() -> dict:
         return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
 
 
-KERNEL_SOURCES = ("attn_tc.cu", "attn_common.cuh", "common.cuh")
+KERNEL_SOURCES = ("attn_tc.cuh", "attn_tc.cu", "attn_tc_e4m3.cu", "attn_common.cuh", "common.cuh")
 
 
 def kernel_source_sha() -> str:
@@ -239,10 +247,17 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     wl = make_workload(args.config, rank, args.reqs, args.seed_offset)
-    dw = P.DeviceWorkload(wl, dev, pin_host=not args.no_e2e, sentinel=False)
+    e4m3 = args.kv == "e4m3"
+    if e4m3:
+        from workloads import page_scales
+        dw = P.DeviceWorkload(wl, dev, pin_host=not args.no_e2e, sentinel=False, kv="e4m3",
+                              page_scales=page_scales(wl))
+    else:
+        dw = P.DeviceWorkload(wl, dev, pin_host=not args.no_e2e, sentinel=False)
     step_i = len(wl.steps) - 1
     ds = dw.steps[step_i]
-    acc = accounting(wl, wl.steps[step_i])
+    acc = accounting(wl, wl.steps[step_i], e4m3)
+    workload_name = wl.name + ("_e4m3kv" if e4m3 else "")
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
         dw.run_fill(stream)
@@ -253,7 +268,9 @@ def run_ours(args, rank, world, local):
     ws_bytes = ds.workspace.numel() if ds.workspace is not None else 0
     merges = 1 if N.yoco_cross_attn_workspace_size(max(ds.rows_upper, 1), wl.num_q_heads,
                                                    wl.num_kv_heads, wl.head_dim, wl.block_size,
-                                                   ds.max_seq_len, P.torch_dtype(wl.dtype)) > 0 else 0
+                                                   ds.max_seq_len,
+                                                   torch.float8_e4m3fn if e4m3
+                                                   else P.torch_dtype(wl.dtype)) > 0 else 0
     launches_per_step = 2 + wl.layers * (1 + merges)
 
     sampler = None if args.no_clocks else ClockSampler(local)
@@ -347,14 +364,15 @@ def run_ours(args, rank, world, local):
     value = total_kv_bytes / (max_ms / 1e3) / 1e9
     peaks = measured_peaks()
     achieved = acc["attn_bytes_layer"] / (attn_launch_ms / 1e3) / 1e9
-    traffic = profiled_traffic(wl.name)
+    traffic = profiled_traffic(workload_name)
     res = {
         "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 cache, bf16 q/out, f16 mma" if e4m3 else wl.dtype,
         "data": "synthetic (seeded N(0,1) K/V and queries, random page permutation)",
         "config": {
-            "workload": wl.name, "description": wl.description, "H_q": wl.num_q_heads,
+            "workload": workload_name, "description": wl.description, "H_q": wl.num_q_heads,
             "H_kv": wl.num_kv_heads, "head_dim": wl.head_dim, "block_size": wl.block_size,
             "layers": wl.layers, "requests": wl.steps[step_i].num_reqs,
             "step_tokens": wl.steps[step_i].num_tokens, "cross_rows": acc["rows"],
@@ -375,7 +393,7 @@ def run_ours(args, rank, world, local):
     }
     if e2e is not None:
         res["e2e"] = e2e
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not e4m3:
         res["cpu_baseline"] = cpu_baseline(wl, step_i)
     return res
 

@@ -67,7 +67,10 @@ typedef enum {
     YOCO_ERR_CUDA = 4         /* a CUDA runtime call or kernel launch failed */
 } yoco_status_t;
 
-typedef enum { YOCO_F32 = 0, YOCO_BF16 = 1 } yoco_dtype_t;
+/* YOCO_E4M3 names the 8-bit cache of the *_e4m3 calls (bf16 queries and
+ * outputs over an e4m3 cache); only yoco_cross_attn_workspace_size and
+ * yoco_cross_decoder_bytes take it. */
+typedef enum { YOCO_F32 = 0, YOCO_BF16 = 1, YOCO_E4M3 = 2 } yoco_dtype_t;
 
 /* Flags of yoco_cross_attn_paged. */
 #define YOCO_ATTN_REVERSE 0x1u /* bf16 path: walk each worker's pages last to first (see below) */
@@ -78,6 +81,7 @@ typedef enum { YOCO_F32 = 0, YOCO_BF16 = 1 } yoco_dtype_t;
 #define YOCO_DEVERR_EMPTY_ROW 0x4    /* a cross row with no key to attend (seq_len < rows of its request) */
 #define YOCO_DEVERR_OFFSETS 0x8      /* query_start_loc decreasing, or rows_per_req negative */
 #define YOCO_DEVERR_TIMEOUT 0x10     /* a bounded wait on an asynchronous copy gave up */
+#define YOCO_DEVERR_SCALE 0x20       /* e4m3 cache: a page scale outside the supported range */
 
 /*
  * yoco_kv_append — write the step's new shared K^/V^ into the paged cache.
@@ -131,7 +135,8 @@ yoco_status_t yoco_select_cross_rows(const int32_t* query_start_loc, const int32
  * yoco_cross_attn_workspace_size — bytes of fp32 scratch that
  * yoco_cross_attn_paged needs for these bounds on the current device (the
  * split-KV partial outputs and their log-sum-exp statistics). Returns 0 for
- * unsupported or invalid arguments.
+ * unsupported or invalid arguments. dtype YOCO_E4M3 sizes the scratch of
+ * yoco_cross_attn_paged_e4m3.
  */
 size_t yoco_cross_attn_workspace_size(int32_t max_rows, int32_t num_q_heads, int32_t num_kv_heads,
                                       int32_t head_dim, int32_t block_size, int32_t max_seq_len,
@@ -178,6 +183,72 @@ yoco_status_t yoco_cross_attn_paged(const void* q, const void* k_cache, const vo
                                     int32_t num_blocks, float scale, yoco_dtype_t dtype,
                                     uint32_t flags, void* workspace, size_t workspace_bytes,
                                     int32_t* err_word, void* stream);
+
+/*
+ * 8-bit cache: e4m3 K^/V^ with a K and a V scale per (page, kv head)
+ * ---------------------------------------------------------------------
+ * "KV cache memory systems", "Quantized cache changes attention inputs": a
+ * quantized cache cuts the bytes per cached scalar and adds scale metadata;
+ * keys and values may need separate calibration, per head. In YOCO the one
+ * shared cache is what every cross-decoder layer streams ("YOCO 论文与推理
+ * 数据流详解" §11, §18.2), so halving its bytes halves each layer's traffic;
+ * one cache serves all layers, so there is no per-layer scale.
+ *   - Pools hold one e4m3 byte per element (1 sign, 4 exponent bits with
+ *     bias 7, 3 mantissa bits; largest finite 448; no infinities), in the
+ *     layout above.
+ *   - page_scales is device float32 [num_blocks][num_kv_heads][4]: the record
+ *     of (page, kv head) is {k_scale, v_scale, unused, unused} (16 bytes, so
+ *     one asynchronous copy fetches it with its page). Code c stands for
+ *     value(c) * scale. The caller chooses the scales (calibration); a page
+ *     keeps its scales while it holds tokens.
+ *   - head_dim 128 or 256; block_size 16 or 32; groups up to 16 (as above).
+ */
+
+/*
+ * yoco_kv_append_e4m3 — yoco_kv_append for an e4m3 cache: each element of
+ * a new token's K^ (V^) row is stored as the e4m3 code nearest to
+ * value / k_scale (value / v_scale) of its page and kv head, the division
+ * in float32, ties to the even code, saturating at +-448.
+ *   k_new, v_new   device bf16 [num_tokens][num_kv_heads][head_dim], 16-byte aligned
+ *   k_cache, v_cache  device uint8 pools, 16-byte aligned
+ *   page_scales    device float32 records (above), 16-byte aligned
+ * A (token, kv head) whose page scale is not a positive finite number is
+ * not written and sets YOCO_DEVERR_SCALE. Other arguments, checks and
+ * device-side errors are those of yoco_kv_append.
+ */
+yoco_status_t yoco_kv_append_e4m3(const void* k_new, const void* v_new, void* k_cache,
+                                  void* v_cache, const float* page_scales,
+                                  const int32_t* block_table, int32_t max_blocks_per_req,
+                                  const int32_t* seq_lens, const int32_t* query_start_loc,
+                                  int32_t num_reqs, int32_t num_tokens, int32_t num_blocks,
+                                  int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                                  int32_t* err_word, void* stream);
+
+/*
+ * yoco_cross_attn_paged_e4m3 — yoco_cross_attn_paged over an e4m3 cache.
+ * Computes out = softmax(scale * q K^T) V with K = value(code) * k_scale and
+ * V = value(code) * v_scale of each key's page and kv head.
+ *   q, out        device bf16 [max_rows][num_q_heads][head_dim]
+ *   k_cache, v_cache, page_scales  as for yoco_kv_append_e4m3
+ *   workspace     >= yoco_cross_attn_workspace_size(..., YOCO_E4M3) bytes
+ * Scales must lie in [2^-16, 2^7]; a page read with a scale outside that
+ * range (or not finite) sets YOCO_DEVERR_SCALE and its result is undefined.
+ * Arithmetic: codes widen exactly to f16, queries round to f16 (finite
+ * queries must stay below 65504 in magnitude), f16 tensor-core products
+ * with fp32 accumulation, f16 probabilities, and the V scale applied per
+ * page in fp32. Everything else (flags, errors, determinism) is as for
+ * yoco_cross_attn_paged.
+ */
+yoco_status_t yoco_cross_attn_paged_e4m3(const void* q, const void* k_cache, const void* v_cache,
+                                         const float* page_scales, void* out,
+                                         const int32_t* block_table, int32_t max_blocks_per_req,
+                                         const int32_t* seq_lens,
+                                         const int32_t* cross_query_start_loc, int32_t num_reqs,
+                                         int32_t max_rows, int32_t max_seq_len,
+                                         int32_t num_q_heads, int32_t num_kv_heads,
+                                         int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                         float scale, uint32_t flags, void* workspace,
+                                         size_t workspace_bytes, int32_t* err_word, void* stream);
 
 /*
  * yoco_cross_attn_paged_noalloc — yoco_cross_attn_paged for callers that
@@ -236,7 +307,9 @@ yoco_status_t yoco_set_l2_window(void* stream, void* base, size_t bytes, float h
  *   layers * sum_i ( kv_i * 2 * H_kv * head_dim * elem      K^ and V^
  *                  + 2 * H_q * head_dim * elem               query and output
  *                  + 4 * ceil(kv_i / block_size) * H_kv )    block-table entries
- * with elem = 2 (bf16) or 4 (fp32) and kv_i clamped at 0.
+ * with elem = 2 (bf16) or 4 (fp32) and kv_i clamped at 0. For YOCO_E4M3 the
+ * K^/V^ term uses 1 byte per element, the query/output term 2, and each page
+ * adds its 16-byte scale record next to its block-table entry.
  *   query_start_loc, seq_lens   host int32 [num_reqs + 1] / [num_reqs]
  *   rows_per_req                host int32 [num_reqs] or NULL (= 1)
  *   per_req_bytes               host int64 out [num_reqs] or NULL

@@ -93,3 +93,51 @@ def test_workspace_sizes(lib_path):
     b = N.yoco_cross_attn_workspace_size(64, 16, 1, 128, 32, 131072, torch.bfloat16)
     assert a == b > 0
     assert N.yoco_cross_attn_workspace_size(4, 16, 1, 96, 32, 4096, torch.bfloat16) == 0
+
+
+def test_e4m3_host_validation(lib_path):
+    from yoco_shared_kv_gb300 import _native as N
+    L = N.lib
+    fake = 1 << 20  # never dereferenced: every call below returns before a launch
+
+    def attn(**kw):
+        a = dict(hq=8, hkv=2, d=256, bs=16, sc=fake, flags=0)
+        a.update(kw)
+        return L.yoco_cross_attn_paged_e4m3(fake, fake, fake, a["sc"], fake, fake, 4, fake, fake,
+                                            1, 1, 64, a["hq"], a["hkv"], a["d"], a["bs"], 100,
+                                            0.0625, a["flags"], None, 0, None, None)
+    assert attn(d=64) == N.YOCO_ERR_UNSUPPORTED     # e4m3 pages need 128-byte rows
+    assert attn(bs=8) == N.YOCO_ERR_UNSUPPORTED
+    assert attn(sc=None) == N.YOCO_ERR_INVALID_ARG  # scale records are required
+    assert attn(sc=fake + 8) == N.YOCO_ERR_INVALID_ARG  # 16-byte records, 16-byte aligned
+    assert attn(flags=0x4) == N.YOCO_ERR_INVALID_ARG
+    assert attn() == N.YOCO_ERR_WORKSPACE           # no workspace given
+    # the bf16 entry refuses the e4m3 dtype
+    assert L.yoco_cross_attn_paged(fake, fake, fake, fake, fake, 4, fake, fake, 1, 1, 64, 8, 2,
+                                   256, 16, 100, 0.0625, N.YOCO_E4M3, 0, None, 0, None,
+                                   None) == N.YOCO_ERR_UNSUPPORTED
+
+    def app(**kw):
+        a = dict(d=128, sc=fake)
+        a.update(kw)
+        return L.yoco_kv_append_e4m3(fake, fake, fake, fake, a["sc"], fake, 4, fake, fake, 1, 1,
+                                     100, 16, 2, a["d"], None, None)
+    assert app(d=64) == N.YOCO_ERR_UNSUPPORTED
+    assert app(sc=None) == N.YOCO_ERR_INVALID_ARG
+    assert app(sc=fake + 4) == N.YOCO_ERR_INVALID_ARG
+
+
+def test_e4m3_workspace_and_traffic(lib_path):
+    from yoco_shared_kv_gb300 import _native as N
+    import torch
+    f8 = torch.float8_e4m3fn
+    assert N.yoco_cross_attn_workspace_size(4, 8, 2, 64, 16, 4096, f8) == 0
+    a = N.yoco_cross_attn_workspace_size(4, 8, 2, 256, 16, 4096, f8)
+    b = N.yoco_cross_attn_workspace_size(64, 8, 2, 256, 16, 131072, f8)
+    assert a == b > 0
+    # one request, one row over 100 keys: K/V bytes halve, scale records are added
+    tb, _ = N.yoco_cross_decoder_bytes([0, 1], None, [100], 1, 8, 2, 128, 16, torch.bfloat16)
+    t8, _ = N.yoco_cross_decoder_bytes([0, 1], None, [100], 1, 8, 2, 128, 16, f8)
+    pages = 7
+    assert tb == 100 * 2 * 2 * 128 * 2 + 2 * 8 * 128 * 2 + 4 * pages * 2
+    assert t8 == 100 * 2 * 2 * 128 * 1 + 2 * 8 * 128 * 2 + 20 * pages * 2

@@ -18,19 +18,21 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libyoco_kv.so")
 
 YOCO_OK, YOCO_ERR_INVALID_ARG, YOCO_ERR_UNSUPPORTED, YOCO_ERR_WORKSPACE, YOCO_ERR_CUDA = range(5)
-YOCO_F32, YOCO_BF16 = 0, 1
+YOCO_F32, YOCO_BF16, YOCO_E4M3 = 0, 1, 2
 YOCO_ATTN_REVERSE = 0x1
 DEVERR_PAGE_RANGE = 0x1
 DEVERR_POS_RANGE = 0x2
 DEVERR_EMPTY_ROW = 0x4
 DEVERR_OFFSETS = 0x8
 DEVERR_TIMEOUT = 0x10
+DEVERR_SCALE = 0x20
 
 EXPORTED = ("yoco_kv_append", "yoco_select_cross_rows", "yoco_cross_attn_workspace_size",
             "yoco_cross_attn_paged", "yoco_set_l2_window", "yoco_status_string", "yoco_version",
             "yoco_last_cuda_error", "yoco_last_cuda_error_string",
             "yoco_cross_attn_paged_noalloc", "yoco_cross_attn_noalloc_capacity",
-            "yoco_selftest_wait_timeout", "yoco_cross_decoder_bytes")
+            "yoco_selftest_wait_timeout", "yoco_cross_decoder_bytes", "yoco_kv_append_e4m3",
+            "yoco_cross_attn_paged_e4m3")
 
 
 class YocoError(RuntimeError):
@@ -80,6 +82,13 @@ def _load() -> ctypes.CDLL:
     L.yoco_cross_decoder_bytes.restype = ctypes.c_int64
     L.yoco_cross_decoder_bytes.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, ctypes.c_int,
                                            vp]
+    L.yoco_kv_append_e4m3.restype = ctypes.c_int
+    L.yoco_kv_append_e4m3.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32,
+                                      i32, vp, vp]
+    L.yoco_cross_attn_paged_e4m3.restype = ctypes.c_int
+    L.yoco_cross_attn_paged_e4m3.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32,
+                                             i32, i32, i32, i32, i32, ctypes.c_float,
+                                             ctypes.c_uint32, vp, sz, vp, vp]
     return L
 
 
@@ -96,10 +105,13 @@ def _check(fn: str, status: int) -> None:
 
 
 def dtype_code(t: torch.dtype) -> int:
+    """bf16 / fp32 caches; torch.float8_e4m3fn (or uint8) names the e4m3 cache."""
     if t == torch.bfloat16:
         return YOCO_BF16
     if t == torch.float32:
         return YOCO_F32
+    if t in (torch.float8_e4m3fn, torch.uint8):
+        return YOCO_E4M3
     raise ValueError(f"unsupported dtype {t}")
 
 
@@ -252,3 +264,50 @@ def yoco_last_cuda_error() -> int:
 
 def yoco_last_cuda_error_string() -> str:
     return lib.yoco_last_cuda_error_string().decode()
+
+
+def yoco_kv_append_e4m3(k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+                        v_cache: torch.Tensor, page_scales: torch.Tensor, block_table: torch.Tensor,
+                        seq_lens: torch.Tensor, query_start_loc: torch.Tensor,
+                        err_word: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Quantising append: bf16 ``k_new/v_new [T, H_kv, D]`` into one-byte pools
+    ``[num_blocks, H_kv, bs, D]`` with float32 ``page_scales [num_blocks, H_kv, 4]``."""
+    num_blocks, H_kv, bs, D = k_cache.shape
+    assert v_cache.shape == k_cache.shape and k_new.shape == v_new.shape
+    assert k_new.dtype == v_new.dtype == torch.bfloat16
+    assert k_cache.element_size() == 1 and v_cache.element_size() == 1
+    assert page_scales.dtype == torch.float32 and tuple(page_scales.shape) == (num_blocks, H_kv, 4)
+    T = k_new.shape[0]
+    assert k_new.shape[1:] == (H_kv, D)
+    R = query_start_loc.shape[0] - 1
+    _check("yoco_kv_append_e4m3", lib.yoco_kv_append_e4m3(
+        _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(page_scales),
+        _i32(block_table, "block_table"), block_table.shape[1], _i32(seq_lens, "seq_lens"),
+        _i32(query_start_loc, "query_start_loc"), R, T, num_blocks, bs, H_kv, D,
+        None if err_word is None else _i32(err_word, "err_word"), _stream(stream)))
+
+
+def yoco_cross_attn_paged_e4m3(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                               page_scales: torch.Tensor, out: torch.Tensor,
+                               block_table: torch.Tensor, seq_lens: torch.Tensor,
+                               cross_query_start_loc: torch.Tensor, max_seq_len: int, scale: float,
+                               workspace: Optional[torch.Tensor],
+                               err_word: Optional[torch.Tensor] = None, stream=None,
+                               max_rows: Optional[int] = None, flags: int = 0) -> None:
+    """One layer over an e4m3 cache: bf16 ``q/out [max_rows, H_q, D]``."""
+    num_blocks, H_kv, bs, D = k_cache.shape
+    rows_cap, H_q, Dq = q.shape
+    assert Dq == D and out.shape == q.shape and out.dtype == q.dtype == torch.bfloat16
+    assert k_cache.element_size() == 1 and v_cache.shape == k_cache.shape
+    assert page_scales.dtype == torch.float32 and tuple(page_scales.shape) == (num_blocks, H_kv, 4)
+    R = cross_query_start_loc.shape[0] - 1
+    max_rows = rows_cap if max_rows is None else max_rows
+    assert max_rows <= rows_cap
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("yoco_cross_attn_paged_e4m3", lib.yoco_cross_attn_paged_e4m3(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_scales), _ptr(out),
+        _i32(block_table, "block_table"), block_table.shape[1], _i32(seq_lens, "seq_lens"),
+        _i32(cross_query_start_loc, "cross_query_start_loc"), R, max_rows, int(max_seq_len), H_q,
+        H_kv, D, bs, num_blocks, float(scale), int(flags), _ptr(workspace), ws_bytes,
+        None if err_word is None else _i32(err_word, "err_word"), _stream(stream)))
+

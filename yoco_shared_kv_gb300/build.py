@@ -17,8 +17,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libyoco_kv.so")
-SOURCES = ["abi.cu", "kv_append.cu", "select_rows.cu", "cross_attn.cu", "attn_tc.cu", "attn_cc.cu",
-           "attn_static.cu"]
+SOURCES = ["abi.cu", "kv_append.cu", "select_rows.cu", "cross_attn.cu", "attn_tc.cu",
+           "attn_tc_e4m3.cu", "attn_cc.cu", "attn_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", f"-I{INCLUDE}"]

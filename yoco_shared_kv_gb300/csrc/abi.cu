@@ -96,11 +96,15 @@ extern "C" int64_t yoco_cross_decoder_bytes(const int32_t* query_start_loc,
                                             int32_t num_kv_heads, int32_t head_dim,
                                             int32_t block_size, yoco_dtype_t dtype,
                                             int64_t* per_req_bytes) {
+    const bool e4m3 = dtype == YOCO_E4M3;
     if (num_reqs < 0 || layers < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
-        block_size <= 0 || !yoco::dtype_ok(dtype))
+        block_size <= 0 || !(yoco::dtype_ok(dtype) || e4m3))
         return -1;
     if (num_reqs > 0 && (query_start_loc == nullptr || seq_lens == nullptr)) return -1;
-    const int64_t elem = static_cast<int64_t>(yoco::elem_size(dtype));
+    // e4m3: one-byte keys/values, bf16 queries/outputs, a 16-byte scale record per page
+    const int64_t elem = e4m3 ? 2 : static_cast<int64_t>(yoco::elem_size(dtype));
+    const int64_t kv_elem = e4m3 ? 1 : elem;
+    const int64_t page_meta = 4 + (e4m3 ? 16 : 0);
     int64_t total = 0;
     for (int32_t r = 0; r < num_reqs; ++r) {
         const int64_t q_len = static_cast<int64_t>(query_start_loc[r + 1]) - query_start_loc[r];
@@ -111,8 +115,8 @@ extern "C" int64_t yoco_cross_decoder_bytes(const int32_t* query_start_loc,
         for (int64_t i = 0; i < k; ++i) {
             int64_t kv = static_cast<int64_t>(seq_lens[r]) - k + i + 1;
             if (kv < 0) kv = 0;
-            b += kv * 2 * num_kv_heads * head_dim * elem + 2ll * num_q_heads * head_dim * elem +
-                 4 * ((kv + block_size - 1) / block_size) * num_kv_heads;
+            b += kv * 2 * num_kv_heads * head_dim * kv_elem + 2ll * num_q_heads * head_dim * elem +
+                 page_meta * ((kv + block_size - 1) / block_size) * num_kv_heads;
         }
         b *= layers;
         if (per_req_bytes) per_req_bytes[r] = b;

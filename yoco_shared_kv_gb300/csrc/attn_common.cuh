@@ -23,6 +23,7 @@ struct AttnParams {
     int32_t block_size;
     int32_t split_pages;        // CUDA-core path: logical pages per split
     int32_t max_splits;         // CUDA-core path
+    const float4* scales;       // e4m3 cache: {k_scale, v_scale, -, -} per (page, kv head)
     float scale_log2;           // softmax scale * log2(e)
     int32_t reverse;            // tensor-core path: walk each worker's pages from the end
 };
@@ -46,10 +47,12 @@ __device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float x) {
 
 // Host-side launchers (one per path). `tc_workspace_bytes` / `cc_*` give the
 // scratch each path needs.
-size_t tc_workspace_bytes(int sms, int H_kv, int G, int D, int BS);
+size_t tc_workspace_bytes(int sms, int H_kv, int G, int D, int BS, bool e4m3);
 int tc_ctas(int sms);
 cudaError_t launch_attn_tc(const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p,
                            int D, int BS, int sms, cudaStream_t s);
+cudaError_t launch_attn_tc_e4m3(const CUtensorMap& mk, const CUtensorMap& mv,
+                                const AttnParams& p, int D, int BS, int sms, cudaStream_t s);
 cudaError_t launch_attn_cc(const void* k_cache, const void* v_cache, const AttnParams& p, int D,
                            int hb, cudaStream_t s);
 

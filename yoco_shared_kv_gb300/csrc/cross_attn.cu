@@ -1,8 +1,9 @@
 // C entry points of the cross-decoder attention: argument checks, the split
 // plan of the fp32 path, the pools' TMA descriptors and the launch.
 //
-// bf16 runs on the persistent tensor-core path (attn_tc.cu); fp32 runs on
-// the CUDA-core split-KV path (attn_cc.cu).
+// bf16 runs on the persistent tensor-core path (attn_tc.cu), an e4m3 cache
+// on the same path with one-byte pages (attn_tc_e4m3.cu); fp32 runs on the
+// CUDA-core split-KV path (attn_cc.cu).
 #include <mutex>
 
 #include "attn_common.cuh"
@@ -22,17 +23,19 @@ struct Plan {
 
 bool make_plan(yoco_dtype_t dt, int max_rows, int H_q, int H_kv, int D, int BS, int max_seq_len,
                Plan& pl) {
-    if (!dtype_ok(dt) || !head_dim_ok(D) || !block_size_ok(BS)) return false;
+    const bool e4m3 = dt == YOCO_E4M3;
+    if (!(dtype_ok(dt) || e4m3) || !head_dim_ok(D) || !block_size_ok(BS)) return false;
+    if (e4m3 && D == 64) return false;  // e4m3 pages need 128-byte rows
     if (H_q <= 0 || H_kv <= 0 || H_q % H_kv != 0 || H_q / H_kv > 16) return false;
     if (max_rows < 0 || max_seq_len <= 0) return false;
     const int G = H_q / H_kv;
     const int sms = device_sm_count();
-    pl.tc = (dt == YOCO_BF16);
+    pl.tc = (dt == YOCO_BF16 || e4m3);
     pl.hb = 1;
     pl.split_pages = 0;
     pl.max_splits = 1;
     if (pl.tc) {
-        pl.ws_bytes = tc_workspace_bytes(sms, H_kv, G, D, BS);
+        pl.ws_bytes = tc_workspace_bytes(sms, H_kv, G, D, BS, e4m3);
         return true;
     }
     for (int c : {8, 4, 2, 1})
@@ -78,27 +81,29 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// Pool [num_blocks * H_kv * BS rows][D] bf16 as a 2-D tensor; box = 64 elements
-// (128 bytes) x BS rows with the 128-byte swizzle.
-bool encode_pool(CUtensorMap* map, const void* pool, int64_t rows, int D, int BS) {
+// Pool [num_blocks * H_kv * BS rows][D] as a 2-D tensor of bf16 (esz 2) or
+// bytes (esz 1); box = 128 bytes x BS rows with the 128-byte swizzle.
+bool encode_pool(CUtensorMap* map, const void* pool, int64_t rows, int D, int BS, int esz) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
-    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(BS)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * esz};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(BS)};
     const cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides, box,
+    const CUtensorMapDataType ty =
+        esz == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    return fn(map, ty, 2, const_cast<void*>(pool), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Small cache of encoded pool descriptors: the pools of a serving engine are
 // fixed, so each is encoded once instead of on every call.
-bool pool_map(CUtensorMap* map, const void* pool, int64_t rows, int D, int BS) {
+bool pool_map(CUtensorMap* map, const void* pool, int64_t rows, int D, int BS, int esz) {
     struct Entry {
         const void* pool;
         int64_t rows;
-        int D, BS, dev;
+        int D, BS, esz, dev;
         CUtensorMap map;
     };
     static Entry cache[16];
@@ -110,18 +115,19 @@ bool pool_map(CUtensorMap* map, const void* pool, int64_t rows, int D, int BS) {
         std::lock_guard<std::mutex> lock(mu);
         for (int i = 0; i < used; ++i)
             if (cache[i].pool == pool && cache[i].rows == rows && cache[i].D == D &&
-                cache[i].BS == BS && cache[i].dev == dev) {
+                cache[i].BS == BS && cache[i].esz == esz && cache[i].dev == dev) {
                 *map = cache[i].map;
                 return true;
             }
     }
-    if (!encode_pool(map, pool, rows, D, BS)) return false;
+    if (!encode_pool(map, pool, rows, D, BS, esz)) return false;
     std::lock_guard<std::mutex> lock(mu);
     Entry& e = cache[next];
     e.pool = pool;
     e.rows = rows;
     e.D = D;
     e.BS = BS;
+    e.esz = esz;
     e.dev = dev;
     e.map = *map;
     next = (next + 1) % 16;
@@ -152,16 +158,23 @@ extern "C" size_t yoco_cross_attn_workspace_size(int32_t max_rows, int32_t num_q
     return pl.ws_bytes;
 }
 
-extern "C" yoco_status_t yoco_cross_attn_paged(
-    const void* q, const void* k_cache, const void* v_cache, void* out, const int32_t* block_table,
-    int32_t max_blocks_per_req, const int32_t* seq_lens, const int32_t* cross_query_start_loc,
-    int32_t num_reqs, int32_t max_rows, int32_t max_seq_len, int32_t num_q_heads,
-    int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale,
-    yoco_dtype_t dtype, uint32_t flags, void* workspace, size_t workspace_bytes, int32_t* err_word,
-    void* stream) {
-    using namespace yoco;
+namespace yoco {
+namespace {
+
+// Shared body of the attention entry points; dtype YOCO_E4M3 = bf16 queries
+// over an e4m3 cache with its scale records.
+yoco_status_t run_attn(const void* q, const void* k_cache, const void* v_cache,
+                       const float* page_scales, void* out, const int32_t* block_table,
+                       int32_t max_blocks_per_req, const int32_t* seq_lens,
+                       const int32_t* cross_query_start_loc, int32_t num_reqs, int32_t max_rows,
+                       int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                       int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale,
+                       yoco_dtype_t dtype, uint32_t flags, void* workspace,
+                       size_t workspace_bytes, int32_t* err_word, void* stream) {
+    const bool e4m3 = dtype == YOCO_E4M3;
     if (flags & ~static_cast<uint32_t>(YOCO_ATTN_REVERSE)) return YOCO_ERR_INVALID_ARG;
-    if (!dtype_ok(dtype) || !head_dim_ok(head_dim) || !block_size_ok(block_size))
+    if (!(dtype_ok(dtype) || e4m3) || !head_dim_ok(head_dim) || !block_size_ok(block_size) ||
+        (e4m3 && head_dim == 64))
         return YOCO_ERR_UNSUPPORTED;
     if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0)
         return YOCO_ERR_INVALID_ARG;
@@ -172,6 +185,7 @@ extern "C" yoco_status_t yoco_cross_attn_paged(
     if (num_reqs == 0 || max_rows == 0) return YOCO_OK;
     if (!q || !k_cache || !v_cache || !out || !block_table || !seq_lens || !cross_query_start_loc)
         return YOCO_ERR_INVALID_ARG;
+    if (e4m3 && (page_scales == nullptr || !aligned16(page_scales))) return YOCO_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
         (workspace && !aligned16(workspace)))
         return YOCO_ERR_INVALID_ARG;
@@ -202,6 +216,7 @@ extern "C" yoco_status_t yoco_cross_attn_paged(
     p.block_size = block_size;
     p.split_pages = pl.split_pages;
     p.max_splits = pl.max_splits;
+    p.scales = reinterpret_cast<const float4*>(page_scales);
     p.scale_log2 = scale * kLog2e;
     p.reverse = (flags & YOCO_ATTN_REVERSE) ? 1 : 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -211,10 +226,12 @@ extern "C" yoco_status_t yoco_cross_attn_paged(
         p.ws_ml = nullptr;
         CUtensorMap mk, mv;
         const int64_t rows = static_cast<int64_t>(num_blocks) * num_kv_heads * block_size;
-        if (!pool_map(&mk, k_cache, rows, head_dim, block_size) ||
-            !pool_map(&mv, v_cache, rows, head_dim, block_size))
+        const int esz = e4m3 ? 1 : 2;
+        if (!pool_map(&mk, k_cache, rows, head_dim, block_size, esz) ||
+            !pool_map(&mv, v_cache, rows, head_dim, block_size, esz))
             return cuda_status(cudaErrorInvalidValue);  // descriptor encoding refused
-        e = launch_attn_tc(mk, mv, p, head_dim, block_size, device_sm_count(), s);
+        e = e4m3 ? launch_attn_tc_e4m3(mk, mv, p, head_dim, block_size, device_sm_count(), s)
+                 : launch_attn_tc(mk, mv, p, head_dim, block_size, device_sm_count(), s);
     } else {
         p.ws_o = static_cast<float*>(workspace);
         p.ws_ml = pl.max_splits > 1
@@ -225,4 +242,34 @@ extern "C" yoco_status_t yoco_cross_attn_paged(
         e = launch_attn_cc(k_cache, v_cache, p, head_dim, pl.hb, s);
     }
     return cuda_status(e);
+}
+
+}  // namespace
+}  // namespace yoco
+
+extern "C" yoco_status_t yoco_cross_attn_paged(
+    const void* q, const void* k_cache, const void* v_cache, void* out, const int32_t* block_table,
+    int32_t max_blocks_per_req, const int32_t* seq_lens, const int32_t* cross_query_start_loc,
+    int32_t num_reqs, int32_t max_rows, int32_t max_seq_len, int32_t num_q_heads,
+    int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale,
+    yoco_dtype_t dtype, uint32_t flags, void* workspace, size_t workspace_bytes, int32_t* err_word,
+    void* stream) {
+    if (dtype == YOCO_E4M3) return YOCO_ERR_UNSUPPORTED;  // the e4m3 cache has its own entry
+    return yoco::run_attn(q, k_cache, v_cache, nullptr, out, block_table, max_blocks_per_req,
+                          seq_lens, cross_query_start_loc, num_reqs, max_rows, max_seq_len,
+                          num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                          dtype, flags, workspace, workspace_bytes, err_word, stream);
+}
+
+extern "C" yoco_status_t yoco_cross_attn_paged_e4m3(
+    const void* q, const void* k_cache, const void* v_cache, const float* page_scales, void* out,
+    const int32_t* block_table, int32_t max_blocks_per_req, const int32_t* seq_lens,
+    const int32_t* cross_query_start_loc, int32_t num_reqs, int32_t max_rows, int32_t max_seq_len,
+    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+    int32_t num_blocks, float scale, uint32_t flags, void* workspace, size_t workspace_bytes,
+    int32_t* err_word, void* stream) {
+    return yoco::run_attn(q, k_cache, v_cache, page_scales, out, block_table, max_blocks_per_req,
+                          seq_lens, cross_query_start_loc, num_reqs, max_rows, max_seq_len,
+                          num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                          YOCO_E4M3, flags, workspace, workspace_bytes, err_word, stream);
 }

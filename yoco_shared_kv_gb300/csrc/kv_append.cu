@@ -5,6 +5,10 @@
 // cache. "KV cache memory systems", "Contiguous allocation wastes capacity":
 // a token's logical block resolves to a physical page through the block table.
 //
+// The e4m3 variant ("KV cache memory systems", "Quantized cache changes
+// attention inputs") stores each element as an 8-bit code of value / scale,
+// with a K and a V scale per (page, kv head).
+//
 // Design: one warp copies one (token, kv head) row of K and of V, 16 bytes
 // per lane per instruction (a head_dim row is 128..1024 bytes, so a warp
 // covers it in one or two vector loads and stores). The request of a token
@@ -93,6 +97,115 @@ cudaError_t launch_append(const void* k_new, const void* v_new, void* k_cache, v
     return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------- e4m3 cache
+
+// Scale records of the 8-bit cache: {k_scale, v_scale, -, -} per (page, kv head).
+__device__ __forceinline__ bool scale_usable(float s) { return s > 0.f && s <= 3.4e38f; }
+
+// Two floats -> two e4m3 codes (nearest, ties to even, saturating to +-448);
+// `lo` in bits 0..7.
+__device__ __forceinline__ uint32_t e4m3x2_rn_sat(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Same row walk as kv_append_kernel; each lane quantises D / 32 consecutive
+// elements of K and of V (value / scale in float32, then the nearest code).
+template <int D>
+__global__ void __launch_bounds__(kAppendWarps * 32)
+    kv_append_e4m3_kernel(const __nv_bfloat16* __restrict__ k_new,
+                          const __nv_bfloat16* __restrict__ v_new, uint8_t* __restrict__ k_cache,
+                          uint8_t* __restrict__ v_cache, const float4* __restrict__ scales,
+                          const int32_t* __restrict__ block_table, int32_t max_blocks,
+                          const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ qsl,
+                          int32_t num_reqs, int32_t num_tokens, int32_t num_blocks,
+                          int32_t block_size, int32_t num_kv_heads, int32_t* err) {
+    constexpr int E = D / 32;  // elements per lane: 4 or 8
+    static_assert(E == 4 || E == 8, "head_dim 128 or 256");
+    const int lane = threadIdx.x & 31;
+    const int64_t total_rows = static_cast<int64_t>(num_tokens) * num_kv_heads;
+    const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * kAppendWarps + (threadIdx.x >> 5);
+    const int64_t wstride = static_cast<int64_t>(gridDim.x) * kAppendWarps;
+    const int32_t last = __ldg(qsl + num_reqs);
+    for (int64_t row = warp0; row < total_rows; row += wstride) {
+        const int32_t tok = static_cast<int32_t>(row / num_kv_heads);
+        const int32_t h = static_cast<int32_t>(row - static_cast<int64_t>(tok) * num_kv_heads);
+        if (tok >= last || __ldg(qsl) > tok) {
+            if (lane == 0) set_err(err, YOCO_DEVERR_OFFSETS);
+            continue;
+        }
+        int32_t lo = 0, hi = num_reqs - 1;
+        while (lo < hi) {
+            const int32_t mid = (lo + hi) >> 1;
+            if (__ldg(qsl + mid + 1) > tok) hi = mid;
+            else lo = mid + 1;
+        }
+        const int32_t q0 = __ldg(qsl + lo), q1 = __ldg(qsl + lo + 1);
+        const int32_t q_len = q1 - q0;
+        const int64_t pos = static_cast<int64_t>(__ldg(seq_lens + lo)) - q_len + (tok - q0);
+        if (q_len <= 0) {
+            if (lane == 0) set_err(err, YOCO_DEVERR_OFFSETS);
+            continue;
+        }
+        if (pos < 0 || pos / block_size >= max_blocks) {
+            if (lane == 0) set_err(err, YOCO_DEVERR_POS_RANGE);
+            continue;
+        }
+        const int32_t page =
+            __ldg(block_table + static_cast<int64_t>(lo) * max_blocks + pos / block_size);
+        if (page < 0 || page >= num_blocks) {
+            if (lane == 0) set_err(err, YOCO_DEVERR_PAGE_RANGE);
+            continue;
+        }
+        const float4 sc = __ldg(scales + static_cast<int64_t>(page) * num_kv_heads + h);
+        if (!scale_usable(sc.x) || !scale_usable(sc.y)) {
+            if (lane == 0) set_err(err, YOCO_DEVERR_SCALE);
+            continue;
+        }
+        const int64_t dst =
+            ((static_cast<int64_t>(page) * num_kv_heads + h) * block_size + pos % block_size) * D +
+            lane * E;
+        const int64_t src = row * D + lane * E;
+        uint32_t kc[E / 4], vc[E / 4];
+        if constexpr (E == 4) {
+            const uint2 kb = __ldcs(reinterpret_cast<const uint2*>(k_new + src));
+            const uint2 vb = __ldcs(reinterpret_cast<const uint2*>(v_new + src));
+            const uint32_t kw[2] = {kb.x, kb.y}, vw[2] = {vb.x, vb.y};
+            uint32_t k16[2], v16[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                k16[i] = e4m3x2_rn_sat(__fdiv_rn(__uint_as_float(kw[i] << 16), sc.x),
+                                       __fdiv_rn(__uint_as_float(kw[i] & 0xFFFF0000u), sc.x));
+                v16[i] = e4m3x2_rn_sat(__fdiv_rn(__uint_as_float(vw[i] << 16), sc.y),
+                                       __fdiv_rn(__uint_as_float(vw[i] & 0xFFFF0000u), sc.y));
+            }
+            kc[0] = k16[0] | (k16[1] << 16);
+            vc[0] = v16[0] | (v16[1] << 16);
+            *reinterpret_cast<uint32_t*>(k_cache + dst) = kc[0];
+            *reinterpret_cast<uint32_t*>(v_cache + dst) = vc[0];
+        } else {
+            const uint4 kb = __ldcs(reinterpret_cast<const uint4*>(k_new + src));
+            const uint4 vb = __ldcs(reinterpret_cast<const uint4*>(v_new + src));
+            const uint32_t kw[4] = {kb.x, kb.y, kb.z, kb.w}, vw[4] = {vb.x, vb.y, vb.z, vb.w};
+            uint32_t k16[4], v16[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                k16[i] = e4m3x2_rn_sat(__fdiv_rn(__uint_as_float(kw[i] << 16), sc.x),
+                                       __fdiv_rn(__uint_as_float(kw[i] & 0xFFFF0000u), sc.x));
+                v16[i] = e4m3x2_rn_sat(__fdiv_rn(__uint_as_float(vw[i] << 16), sc.y),
+                                       __fdiv_rn(__uint_as_float(vw[i] & 0xFFFF0000u), sc.y));
+            }
+            kc[0] = k16[0] | (k16[1] << 16);
+            kc[1] = k16[2] | (k16[3] << 16);
+            vc[0] = v16[0] | (v16[1] << 16);
+            vc[1] = v16[2] | (v16[3] << 16);
+            *reinterpret_cast<uint2*>(k_cache + dst) = make_uint2(kc[0], kc[1]);
+            *reinterpret_cast<uint2*>(v_cache + dst) = make_uint2(vc[0], vc[1]);
+        }
+    }
+}
+
 }  // namespace
 }  // namespace yoco
 
@@ -141,4 +254,47 @@ extern "C" yoco_status_t yoco_kv_append(const void* k_new, const void* v_new, vo
         default: return YOCO_ERR_UNSUPPORTED;
     }
     return cuda_status(e);
+}
+
+extern "C" yoco_status_t yoco_kv_append_e4m3(const void* k_new, const void* v_new, void* k_cache,
+                                             void* v_cache, const float* page_scales,
+                                             const int32_t* block_table,
+                                             int32_t max_blocks_per_req, const int32_t* seq_lens,
+                                             const int32_t* query_start_loc, int32_t num_reqs,
+                                             int32_t num_tokens, int32_t num_blocks,
+                                             int32_t block_size, int32_t num_kv_heads,
+                                             int32_t head_dim, int32_t* err_word, void* stream) {
+    using namespace yoco;
+    if ((head_dim != 128 && head_dim != 256) || !block_size_ok(block_size))
+        return YOCO_ERR_UNSUPPORTED;
+    if (num_reqs < 0 || num_tokens < 0 || num_blocks <= 0 || num_kv_heads <= 0 ||
+        max_blocks_per_req <= 0)
+        return YOCO_ERR_INVALID_ARG;
+    if (num_tokens == 0 || num_reqs == 0) return YOCO_OK;
+    if (!k_new || !v_new || !k_cache || !v_cache || !page_scales || !block_table || !seq_lens ||
+        !query_start_loc)
+        return YOCO_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        !aligned16(page_scales))
+        return YOCO_ERR_INVALID_ARG;
+    const int64_t rows = static_cast<int64_t>(num_tokens) * num_kv_heads;
+    int64_t blocks = (rows + kAppendWarps - 1) / kAppendWarps;
+    const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const auto* kn = static_cast<const __nv_bfloat16*>(k_new);
+    const auto* vn = static_cast<const __nv_bfloat16*>(v_new);
+    auto* kc = static_cast<uint8_t*>(k_cache);
+    auto* vc = static_cast<uint8_t*>(v_cache);
+    const auto* sc = reinterpret_cast<const float4*>(page_scales);
+    if (head_dim == 128)
+        kv_append_e4m3_kernel<128><<<static_cast<unsigned>(blocks), kAppendWarps * 32, 0, s>>>(
+            kn, vn, kc, vc, sc, block_table, max_blocks_per_req, seq_lens, query_start_loc,
+            num_reqs, num_tokens, num_blocks, block_size, num_kv_heads, err_word);
+    else
+        kv_append_e4m3_kernel<256><<<static_cast<unsigned>(blocks), kAppendWarps * 32, 0, s>>>(
+            kn, vn, kc, vc, sc, block_table, max_blocks_per_req, seq_lens, query_start_loc,
+            num_reqs, num_tokens, num_blocks, block_size, num_kv_heads, err_word);
+    return cuda_status(cudaGetLastError());
 }

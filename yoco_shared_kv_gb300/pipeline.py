@@ -36,7 +36,7 @@ def torch_dtype(dtype: str) -> torch.dtype:
 class DeviceStep:
     """Device copies of one step's inputs, plus its outputs and scratch."""
 
-    def __init__(self, wl, step, device, pin_host: bool = False):
+    def __init__(self, wl, step, device, pin_host: bool = False, e4m3: bool = False):
         self.wl, self.step = wl, step
         dev = torch.device(device)
         i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32))  # noqa: E731
@@ -66,9 +66,10 @@ class DeviceStep:
         self.workspace = None
         if step.q is not None:
             self.out = torch.empty_like(self.dev["q"])
-            ws = N.yoco_cross_attn_workspace_size(max(self.rows_upper, 1), wl.num_q_heads,
-                                                  wl.num_kv_heads, wl.head_dim, wl.block_size,
-                                                  self.max_seq_len, torch_dtype(wl.dtype))
+            ws = N.yoco_cross_attn_workspace_size(
+                max(self.rows_upper, 1), wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                wl.block_size, self.max_seq_len,
+                torch.float8_e4m3fn if e4m3 else torch_dtype(wl.dtype))
             # all-ones bytes (NaN as fp32): the library must never read scratch it
             # did not write in the same call, and this makes such a read visible
             self.workspace = torch.full((max(ws, 16),), 255, dtype=torch.uint8, device=dev)
@@ -83,13 +84,31 @@ class DeviceStep:
 
 
 class DeviceWorkload:
+    """``kv="e4m3"`` keeps the cache as e4m3 bytes with per-(page, kv head) scale
+    records ``page_scales`` (float32 numpy ``[num_blocks, H_kv, 4]``); the
+    workload's values must then be bf16."""
+
     def __init__(self, wl, device="cuda", pin_host: bool = False, sentinel: bool = True,
-                 alternate="auto"):
+                 alternate="auto", kv: str = "native", page_scales=None):
         self.wl = wl
         self.device = torch.device(device)
+        self.e4m3 = kv == "e4m3"
+        if kv not in ("native", "e4m3"):
+            raise ValueError(kv)
         tdt = torch_dtype(wl.dtype)
         shape = wl.pool_shape()
-        if sentinel:
+        self.page_scales = None
+        if self.e4m3:
+            if wl.dtype != "bf16":
+                raise ValueError("the e4m3 cache takes bf16 values")
+            if page_scales is None:
+                raise ValueError("an e4m3 cache needs page_scales")
+            self.page_scales = torch.from_numpy(
+                np.ascontiguousarray(page_scales, dtype=np.float32)).to(self.device)
+            fill = 0xFF if sentinel else 0
+            self.k_cache = torch.full(shape, fill, dtype=torch.uint8, device=self.device)
+            self.v_cache = torch.full(shape, fill, dtype=torch.uint8, device=self.device)
+        elif sentinel:
             # all-ones bytes: NaN in both dtypes, so a stray read poisons the output
             self.k_cache = torch.full(shape, -1, dtype=torch.int16 if tdt == torch.bfloat16
                                       else torch.int32, device=self.device).view(tdt)
@@ -106,13 +125,19 @@ class DeviceWorkload:
             l2 = torch.cuda.get_device_properties(self.device).L2_cache_size
             alternate = pool_bytes > l2
         self.alternate = bool(alternate)
-        self.fill = DeviceStep(wl, wl.fill, device, pin_host) if wl.fill is not None else None
-        self.steps: List[DeviceStep] = [DeviceStep(wl, s, device, pin_host) for s in wl.steps]
+        e8 = self.e4m3
+        self.fill = DeviceStep(wl, wl.fill, device, pin_host, e8) if wl.fill is not None else None
+        self.steps: List[DeviceStep] = [DeviceStep(wl, s, device, pin_host, e8) for s in wl.steps]
 
     # ------------------------------------------------------------------ calls
 
     def append(self, ds: DeviceStep, stream=None) -> None:
         d = ds.dev
+        if self.e4m3:
+            N.yoco_kv_append_e4m3(d["k_new"], d["v_new"], self.k_cache, self.v_cache,
+                                  self.page_scales, d["block_table"], d["seq_lens"], d["qsl"],
+                                  self.err, stream)
+            return
         N.yoco_kv_append(d["k_new"], d["v_new"], self.k_cache, self.v_cache, d["block_table"],
                          d["seq_lens"], d["qsl"], self.err, stream)
 
@@ -127,6 +152,12 @@ class DeviceWorkload:
         layer starts on what the previous one left in L2 (when `alternate` is on)."""
         d = ds.dev
         flags = N.YOCO_ATTN_REVERSE if (self.alternate and layer % 2 == 1) else 0
+        if self.e4m3:
+            N.yoco_cross_attn_paged_e4m3(
+                d["q"][layer] if q is None else q, self.k_cache, self.v_cache, self.page_scales,
+                ds.out[layer] if out is None else out, d["block_table"], d["seq_lens"], ds.cqsl,
+                ds.max_seq_len, self.wl.scale, ds.workspace, self.err, stream, flags=flags)
+            return
         N.yoco_cross_attn_paged(d["q"][layer] if q is None else q, self.k_cache, self.v_cache,
                                 ds.out[layer] if out is None else out, d["block_table"],
                                 d["seq_lens"], ds.cqsl, ds.max_seq_len, self.wl.scale,
