@@ -73,7 +73,8 @@ typedef enum {
 typedef enum { YOCO_F32 = 0, YOCO_BF16 = 1, YOCO_E4M3 = 2 } yoco_dtype_t;
 
 /* Flags of yoco_cross_attn_paged. */
-#define YOCO_ATTN_REVERSE 0x1u /* bf16 path: walk each worker's pages last to first (see below) */
+#define YOCO_ATTN_REVERSE 0x1u /* tensor-core paths: walk each worker's pages last to first */
+#define YOCO_ATTN_OVERLAP 0x2u /* tensor-core paths: may start while the previous kernel drains */
 
 /* Bits OR-ed into *err_word by device code. */
 #define YOCO_DEVERR_PAGE_RANGE 0x1   /* block_table entry outside [0, num_blocks) */
@@ -161,11 +162,18 @@ size_t yoco_cross_attn_workspace_size(int32_t max_rows, int32_t num_q_heads, int
  *   max_rows               host bound on the number of rows (grid size)
  *   max_seq_len            host bound on seq_lens (sizes the split-KV grid)
  *   scale                  softmax scale (1/sqrt(head_dim) for the pages' definition)
- *   flags                  0 or YOCO_ATTN_REVERSE. The serial layers re-read one cache
- *                          ("YOCO 论文与推理数据流详解" §11); with the flag set on every other
- *                          layer, a layer starts on the pages the previous one read last,
- *                          which are still in L2. The result is the same up to summation order.
- *                          Ignored on the fp32 path; other bits are rejected.
+ *   flags                  bits of YOCO_ATTN_REVERSE | YOCO_ATTN_OVERLAP (other bits are
+ *                          rejected; both are ignored on the fp32 path).
+ *                          REVERSE: the serial layers re-read one cache ("YOCO 论文与推理
+ *                          数据流详解" §11); with the flag set on every other layer, a layer
+ *                          starts on the pages the previous one read last, which are still
+ *                          in L2. The result is the same up to summation order.
+ *                          OVERLAP: the call is launched as a programmatic dependent of the
+ *                          kernel before it on `stream`, so it reads block_table, seq_lens,
+ *                          cross_query_start_loc and the cache while that kernel drains.
+ *                          Set it only when that kernel writes none of those (for example
+ *                          the previous cross-decoder layer); queries, outputs and the
+ *                          workspace are touched only after that kernel has finished.
  *   workspace              device scratch of >= yoco_cross_attn_workspace_size(...) bytes,
  *                          16-byte aligned; contents need no initialisation
  *   err_word               device int32 or NULL

@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(_PKG, "libyoco_kv.so")
 YOCO_OK, YOCO_ERR_INVALID_ARG, YOCO_ERR_UNSUPPORTED, YOCO_ERR_WORKSPACE, YOCO_ERR_CUDA = range(5)
 YOCO_F32, YOCO_BF16, YOCO_E4M3 = 0, 1, 2
 YOCO_ATTN_REVERSE = 0x1
+YOCO_ATTN_OVERLAP = 0x2
 DEVERR_PAGE_RANGE = 0x1
 DEVERR_POS_RANGE = 0x2
 DEVERR_EMPTY_ROW = 0x4

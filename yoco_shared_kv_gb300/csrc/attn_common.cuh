@@ -26,6 +26,7 @@ struct AttnParams {
     const float4* scales;       // e4m3 cache: {k_scale, v_scale, -, -} per (page, kv head)
     float scale_log2;           // softmax scale * log2(e)
     int32_t reverse;            // tensor-core path: walk each worker's pages from the end
+    int32_t overlap;            // tensor-core path: launch as a programmatic dependent
 };
 
 // Wait limit for one asynchronous page copy before a kernel gives up.

@@ -374,9 +374,10 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
         const int pro = n_my < STAGES ? n_my : STAGES;
         for (int i = 0; i < pro; ++i) issue(i);
     }
-    // Launched as a programmatic dependent of the previous kernel in the
-    // stream: everything above only reads the (unchanging) metadata and the
-    // cache. Queries, outputs and the workspace are touched after this wait.
+    // When launched as a programmatic dependent of the previous kernel in the
+    // stream (the caller allows it only when that kernel writes neither), the
+    // code above reads the metadata and the cache while that kernel drains.
+    // Queries, outputs and the workspace are touched after this wait.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (lane == 0 && warp <= 1) {
         CtaHdr* hp = ws.hdr + blockIdx.x;
@@ -1083,11 +1084,13 @@ cudaError_t launch_one(const CUtensorMap& mk, const CUtensorMap& mv, const AttnP
     const int ctas = tc_ctas(sms);
     AttnParams q = p;  // workspace: outputs of all pieces, then their (m, l), then headers
     q.ws_ml = reinterpret_cast<float2*>(p.ws_o + tc_pieces(ctas, S::NW, p.G) * D);
-    // Both grids are programmatic dependents of the kernel before them: the
-    // split grid runs its metadata prologue while the previous kernel (for
-    // example the previous layer's merge) drains, and the merge grid is
-    // scheduled while the split grid drains; each waits (griddepcontrol.wait)
-    // before it touches data the previous grid produces.
+    // The merge grid is a programmatic dependent of the split grid: it is
+    // scheduled while the split grid drains and waits (griddepcontrol.wait)
+    // before reading its partials. The split grid is one of the kernel before
+    // it only when the caller allows the overlap: it then runs its metadata
+    // prologue and first page copies while that kernel (for example the
+    // previous layer's merge) drains, and waits before it touches queries,
+    // outputs or the workspace.
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -1097,9 +1100,10 @@ cudaError_t launch_one(const CUtensorMap& mk, const CUtensorMap& mv, const AttnP
     cfg.dynamicSmemBytes = S::SMEM;
     cfg.stream = s;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = p.overlap ? 1 : 0;
     e = cudaLaunchKernelEx(&cfg, kernel, mk, mv, q);
     if (e != cudaSuccess) return e;
+    cfg.numAttrs = 1;
     const int msmem = 2 * ctas * p.G * static_cast<int>(sizeof(float));  // factor tables
     const int msmem_max = 2 * ctas * 16 * static_cast<int>(sizeof(float));  // largest group
     if (msmem_max > 48 * 1024) {  // only ever raise the limit above the default

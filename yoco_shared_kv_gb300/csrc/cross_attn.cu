@@ -172,7 +172,8 @@ yoco_status_t run_attn(const void* q, const void* k_cache, const void* v_cache,
                        yoco_dtype_t dtype, uint32_t flags, void* workspace,
                        size_t workspace_bytes, int32_t* err_word, void* stream) {
     const bool e4m3 = dtype == YOCO_E4M3;
-    if (flags & ~static_cast<uint32_t>(YOCO_ATTN_REVERSE)) return YOCO_ERR_INVALID_ARG;
+    if (flags & ~static_cast<uint32_t>(YOCO_ATTN_REVERSE | YOCO_ATTN_OVERLAP))
+        return YOCO_ERR_INVALID_ARG;
     if (!(dtype_ok(dtype) || e4m3) || !head_dim_ok(head_dim) || !block_size_ok(block_size) ||
         (e4m3 && head_dim == 64))
         return YOCO_ERR_UNSUPPORTED;
@@ -219,6 +220,7 @@ yoco_status_t run_attn(const void* q, const void* k_cache, const void* v_cache,
     p.scales = reinterpret_cast<const float4*>(page_scales);
     p.scale_log2 = scale * kLog2e;
     p.reverse = (flags & YOCO_ATTN_REVERSE) ? 1 : 0;
+    p.overlap = (flags & YOCO_ATTN_OVERLAP) ? 1 : 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (pl.tc) {

@@ -149,9 +149,15 @@ class DeviceWorkload:
     def attend(self, ds: DeviceStep, layer: int, stream=None, q: Optional[torch.Tensor] = None,
                out: Optional[torch.Tensor] = None) -> None:
         """One cross-decoder layer. Odd layers walk the pages last to first, so each
-        layer starts on what the previous one left in L2 (when `alternate` is on)."""
+        layer starts on what the previous one left in L2 (when `alternate` is on).
+        Layers after the first overlap their start with the previous layer's end:
+        the kernel before them (the previous layer's merge) writes none of the
+        metadata or cache they read early; the first layer follows the row
+        selection, which writes cross_query_start_loc, so it does not."""
         d = ds.dev
         flags = N.YOCO_ATTN_REVERSE if (self.alternate and layer % 2 == 1) else 0
+        if layer > 0:
+            flags |= N.YOCO_ATTN_OVERLAP
         if self.e4m3:
             N.yoco_cross_attn_paged_e4m3(
                 d["q"][layer] if q is None else q, self.k_cache, self.v_cache, self.page_scales,
