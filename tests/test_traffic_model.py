@@ -53,11 +53,18 @@ def test_model_predicts_measured_dram_bytes(N):
     import bench
     lines = open(os.path.join(ROOT, "profiles", "traffic.txt")).read().splitlines()
     meas = dict(l.split("=", 1) for l in lines if "=" in l and not l.startswith("#"))
-    for cfg, name in ((1, "pure_decode_bf16"), (3, "long_context_bf16")):
+    for cfg, name, e4m3 in ((1, "pure_decode_bf16", False), (3, "long_context_bf16", False),
+                            (1, "pure_decode_bf16_e4m3kv", True),
+                            (3, "long_context_bf16_e4m3kv", True)):
         wl = bench.make_workload(cfg)
-        tot, _ = _model(N, wl, wl.steps[-1])
+        st = wl.steps[-1]
+        dt = torch.float8_e4m3fn if e4m3 else torch.bfloat16
+        tot, _ = N.yoco_cross_decoder_bytes(st.query_start_loc, st.rows_per_req, st.seq_lens,
+                                            wl.layers, wl.num_q_heads, wl.num_kv_heads,
+                                            wl.head_dim, wl.block_size, dt)
         per_layer = tot / wl.layers
-        assert abs(float(meas[name]) / per_layer - 1.0) < 0.005  # within 0.5 %
+        assert per_layer == bench.accounting(wl, st, e4m3)["attn_bytes_layer"]
+        assert abs(float(meas[name]) / per_layer - 1.0) < 0.006, name  # within 0.6 %
 
 
 def test_model_rejects_bad_arguments(N):
