@@ -379,6 +379,24 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
     // code above reads the metadata and the cache while that kernel drains.
     // Queries, outputs and the workspace are touched after this wait.
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (warp == NW - 1) {
+        // rows with no key to attend: zero output, flag (requests spread over the CTAs)
+        __nv_bfloat16* const outz = static_cast<__nv_bfloat16*>(p.out);
+        for (int32_t r = blockIdx.x; r < p.num_reqs; r += gridDim.x) {
+            const int32_t c0 = __ldg(p.cqsl + r), c1 = __ldg(p.cqsl + r + 1);
+            const int32_t seq = __ldg(p.seq_lens + r), k = c1 - c0;
+            for (int32_t n = c0; n < c1 && n < p.max_rows; ++n) {
+                const int32_t kv = seq - k + (n - c0) + 1;
+                if (kv <= 0) {
+                    for (int i = lane; i < p.H_q * D; i += 32)
+                        outz[static_cast<int64_t>(n) * p.H_q * D + i] = __float2bfloat16_rn(0.f);
+                    if (lane == 0) set_err(p.err, YOCO_DEVERR_EMPTY_ROW);
+                } else if (kv > cap && lane == 0) {
+                    set_err(p.err, YOCO_DEVERR_POS_RANGE);
+                }
+            }
+        }
+    }
     if (lane == 0 && warp <= 1) {
         CtaHdr* hp = ws.hdr + blockIdx.x;
         if (warp == 0) {
@@ -894,8 +912,9 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Finishes every segment cut by a CTA boundary from the CTA-level partials,
-// and zero-fills rows that have no key. Grid: one CTA per split-kernel CTA.
+// Finishes every segment cut by a CTA boundary from the CTA-level partials
+// (rows with no key are zero-filled by the split kernel). Grid: one CTA per
+// split-kernel CTA.
 // Each CTA spanned by a cut segment takes an equal share of that segment's
 // G x D outputs, so a long segment's merge spreads over all of its CTAs. A
 // CTA shares at most two segments (those of its first and last page); the
@@ -921,21 +940,6 @@ __global__ void __launch_bounds__(kMergeThreads) attn_tc_merge(const AttnParams 
     const TcWs ws = tc_ws(p, ctas, NW, D);
     const CtaHdr Hc = ws.hdr[c];
 
-    // rows with no key to attend: zero output, flag (requests spread over the CTAs)
-    for (int32_t r = c; r < p.num_reqs; r += ctas) {
-        const int32_t c0 = __ldg(p.cqsl + r), c1 = __ldg(p.cqsl + r + 1);
-        const int32_t seq = __ldg(p.seq_lens + r), k = c1 - c0;
-        for (int32_t n = c0; n < c1 && n < p.max_rows; ++n) {
-            const int32_t kv = seq - k + (n - c0) + 1;
-            if (kv <= 0) {
-                for (int i = threadIdx.x; i < p.H_q * D; i += blockDim.x)
-                    outp[static_cast<int64_t>(n) * p.H_q * D + i] = __float2bfloat16_rn(0.f);
-                if (threadIdx.x == 0) set_err(p.err, YOCO_DEVERR_EMPTY_ROW);
-            } else if (kv > cap && threadIdx.x == 0) {
-                set_err(p.err, YOCO_DEVERR_POS_RANGE);
-            }
-        }
-    }
     if (launch_aborted(p)) return;
     const int64_t P = Hc.P;
     if (P <= 0) return;
