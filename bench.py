@@ -57,6 +57,8 @@ def parse_args(argv=None):
     ap.add_argument("--seed-offset", type=int, default=0)
     ap.add_argument("--kv", choices=["native", "e4m3"], default="native",
                     help="cache format: the workload's dtype, or e4m3 with per-page scales")
+    ap.add_argument("--fused", action="store_true",
+                    help="decode workloads: fuse the append into layer 0 (yoco_cross_decode_step)")
     return ap.parse_args(argv)
 
 
@@ -258,6 +260,14 @@ def run_ours(args, rank, world, local):
     ds = dw.steps[step_i]
     acc = accounting(wl, wl.steps[step_i], e4m3)
     workload_name = wl.name + ("_e4m3kv" if e4m3 else "")
+    if args.fused and not dw.decode_only(step_i):
+        raise SystemExit("--fused needs a decode-only workload (one token and one row per request)")
+
+    def step_fn(i):
+        if args.fused:
+            dw.fused_step(i)
+        else:
+            dw.run_step(i)
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
         dw.run_fill(stream)
@@ -271,7 +281,7 @@ def run_ours(args, rank, world, local):
                                                    ds.max_seq_len,
                                                    torch.float8_e4m3fn if e4m3
                                                    else P.torch_dtype(wl.dtype)) > 0 else 0
-    launches_per_step = 2 + wl.layers * (1 + merges)
+    launches_per_step = (0 if args.fused else 2) + wl.layers * (1 + merges)
 
     sampler = None if args.no_clocks else ClockSampler(local)
     L = wl.layers
@@ -279,11 +289,11 @@ def run_ours(args, rank, world, local):
     # engine replays its captured cross-decoder; a second graph holds only the
     # L attention calls, to time the dominant kernel on its own.
     with torch.cuda.stream(stream):
-        dw.run_step(step_i, stream)  # eager once: one-time host set-up before capture
+        step_fn(step_i)  # eager once: one-time host set-up before capture
     stream.synchronize()
     g_step, g_attn = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_step, stream=stream):
-        dw.run_step(step_i)
+        step_fn(step_i)
     with torch.cuda.graph(g_attn, stream=stream):
         for layer in range(L):
             dw.attend(ds, layer)
@@ -380,6 +390,8 @@ def run_ours(args, rank, world, local):
             "l2": ("inputs larger than L2" if acc["kv_bytes_layer"] > 129e6
                    else "inputs fit in L2 (layers re-read them: logical bytes)"),
             "parallelism": f"replicas x{world}",
+            "step": ("append fused into layer 0 (yoco_cross_decode_step)" if args.fused
+                     else "append, select, every layer"),
         },
         "hbm_frac": round(value / peaks["hbm_gbs"], 4),
         "query_rows_per_s": round(total_rows / (max_ms / 1e3), 1),

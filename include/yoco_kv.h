@@ -259,6 +259,41 @@ yoco_status_t yoco_cross_attn_paged_e4m3(const void* q, const void* k_cache, con
                                          size_t workspace_bytes, int32_t* err_word, void* stream);
 
 /*
+ * yoco_cross_decode_step — a decode step's append and its first cross-decoder
+ * layer in one launch (bf16 or e4m3 cache).
+ *
+ * For a decode-only batch (every request schedules exactly one new token and
+ * gets one cross row, "You Only Cache Once, in vLLM", "Implementation in
+ * vLLM"), this does what yoco_kv_append (or yoco_kv_append_e4m3) followed by
+ * yoco_cross_attn_paged (or yoco_cross_attn_paged_e4m3) does for layer 0:
+ * "YOCO 论文与推理数据流详解" §10.3–§10.4 — the token's K^/V^ is appended
+ * once, and the layer's query attends to the keys up to and including it.
+ * Later layers use yoco_cross_attn_paged(_e4m3) on the same cache.
+ *   k_new, v_new      device bf16 [num_reqs][num_kv_heads][head_dim], 16-byte aligned
+ *   query_start_loc   device int32 [num_reqs + 1] = 0, 1, ..., num_reqs (it is also the
+ *                     cross query_start_loc); a request with another token count sets
+ *                     YOCO_DEVERR_OFFSETS and its result is undefined
+ *   seq_lens          tokens in the cache after this step (the new token included)
+ *   dtype             YOCO_BF16 (page_scales ignored) or YOCO_E4M3 (page_scales as for
+ *                     yoco_kv_append_e4m3); the pools hold that format
+ *   workspace         >= yoco_cross_attn_workspace_size(num_reqs, ..., dtype) bytes
+ * Other arguments, checks and errors are those of yoco_cross_attn_paged; of the flags only
+ * YOCO_ATTN_OVERLAP is taken (YOCO_ATTN_REVERSE is rejected: the step walks its pages
+ * forward). The cache ends bit-identical to the separate append, and the output to the
+ * separate attention.
+ */
+yoco_status_t yoco_cross_decode_step(const void* q, const void* k_new, const void* v_new,
+                                     void* k_cache, void* v_cache, const float* page_scales,
+                                     void* out, const int32_t* block_table,
+                                     int32_t max_blocks_per_req, const int32_t* seq_lens,
+                                     const int32_t* query_start_loc, int32_t num_reqs,
+                                     int32_t max_seq_len, int32_t num_q_heads,
+                                     int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                     int32_t num_blocks, float scale, yoco_dtype_t dtype,
+                                     uint32_t flags, void* workspace, size_t workspace_bytes,
+                                     int32_t* err_word, void* stream);
+
+/*
  * yoco_cross_attn_paged_noalloc — yoco_cross_attn_paged for callers that
  * cannot allocate device memory. The pages have no counterpart: this is a
  * library convenience, not part of the method.

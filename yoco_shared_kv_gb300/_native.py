@@ -33,7 +33,7 @@ EXPORTED = ("yoco_kv_append", "yoco_select_cross_rows", "yoco_cross_attn_workspa
             "yoco_last_cuda_error", "yoco_last_cuda_error_string",
             "yoco_cross_attn_paged_noalloc", "yoco_cross_attn_noalloc_capacity",
             "yoco_selftest_wait_timeout", "yoco_cross_decoder_bytes", "yoco_kv_append_e4m3",
-            "yoco_cross_attn_paged_e4m3")
+            "yoco_cross_attn_paged_e4m3", "yoco_cross_decode_step")
 
 
 class YocoError(RuntimeError):
@@ -86,6 +86,10 @@ def _load() -> ctypes.CDLL:
     L.yoco_kv_append_e4m3.restype = ctypes.c_int
     L.yoco_kv_append_e4m3.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32,
                                       i32, vp, vp]
+    L.yoco_cross_decode_step.restype = ctypes.c_int
+    L.yoco_cross_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32,
+                                         i32, i32, i32, i32, i32, ctypes.c_float, ctypes.c_int,
+                                         ctypes.c_uint32, vp, sz, vp, vp]
     L.yoco_cross_attn_paged_e4m3.restype = ctypes.c_int
     L.yoco_cross_attn_paged_e4m3.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32,
                                              i32, i32, i32, i32, i32, ctypes.c_float,
@@ -311,4 +315,31 @@ def yoco_cross_attn_paged_e4m3(q: torch.Tensor, k_cache: torch.Tensor, v_cache: 
         _i32(cross_query_start_loc, "cross_query_start_loc"), R, max_rows, int(max_seq_len), H_q,
         H_kv, D, bs, num_blocks, float(scale), int(flags), _ptr(workspace), ws_bytes,
         None if err_word is None else _i32(err_word, "err_word"), _stream(stream)))
+
+
+def yoco_cross_decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                           k_cache: torch.Tensor, v_cache: torch.Tensor,
+                           page_scales: Optional[torch.Tensor], out: torch.Tensor,
+                           block_table: torch.Tensor, seq_lens: torch.Tensor,
+                           query_start_loc: torch.Tensor, max_seq_len: int, scale: float,
+                           workspace: Optional[torch.Tensor],
+                           err_word: Optional[torch.Tensor] = None, stream=None,
+                           flags: int = 0) -> None:
+    """Decode step: append ``k_new/v_new [R, H_kv, D]`` and attend layer ``q [R, H_q, D]``."""
+    num_blocks, H_kv, bs, D = k_cache.shape
+    R, H_q, Dq = q.shape
+    assert Dq == D and out.shape == q.shape and q.dtype == torch.bfloat16
+    assert k_new.shape == v_new.shape == (R, H_kv, D) and k_new.dtype == torch.bfloat16
+    assert query_start_loc.shape[0] == R + 1
+    e4m3 = k_cache.element_size() == 1
+    if e4m3:
+        assert page_scales is not None and page_scales.dtype == torch.float32
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("yoco_cross_decode_step", lib.yoco_cross_decode_step(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+        _ptr(page_scales) if e4m3 else None, _ptr(out), _i32(block_table, "block_table"),
+        block_table.shape[1], _i32(seq_lens, "seq_lens"),
+        _i32(query_start_loc, "query_start_loc"), R, int(max_seq_len), H_q, H_kv, D, bs,
+        num_blocks, float(scale), YOCO_E4M3 if e4m3 else YOCO_BF16, int(flags), _ptr(workspace),
+        ws_bytes, None if err_word is None else _i32(err_word, "err_word"), _stream(stream)))
 

@@ -12,6 +12,13 @@ struct AttnParams {
     const int32_t* block_table; // [num_reqs][max_blocks]
     const int32_t* seq_lens;    // [num_reqs]
     const int32_t* cqsl;        // [num_reqs + 1] cross query_start_loc
+    // fused decode step (tensor-core paths): this step's new K^/V^ rows, bf16
+    // [num_reqs][H_kv][D] (one token per request), appended to the pools by the
+    // same launch; null otherwise
+    const void* k_new;
+    const void* v_new;
+    void* k_pool;
+    void* v_pool;
     float* ws_o;                // partial outputs (layout depends on the path)
     float2* ws_ml;              // partial (running max in log2 units, sum)
     int32_t* err;

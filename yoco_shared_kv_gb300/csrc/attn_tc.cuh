@@ -262,7 +262,9 @@ __device__ __forceinline__ TcWs tc_ws(const AttnParams& p, int ctas, int nw, int
 
 // --------------------------------------------------------------- kernel
 
-template <int D, int BS, int NT, bool REV, bool F8>
+// FUSE: fused decode step (append this step's tokens, patch them into the
+// copied pages); instantiated with REV = false only.
+template <int D, int BS, int NT, bool REV, bool F8, bool FUSE>
 __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
     attn_tc_persistent(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
@@ -379,6 +381,53 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
     // code above reads the metadata and the cache while that kernel drains.
     // Queries, outputs and the workspace are touched after this wait.
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (FUSE && warp == NW - 1) {
+        // fused decode step: append each request's one new token (requests spread
+        // over the CTAs; after the wait, so no earlier kernel still reads the pools)
+        constexpr int CH = F8 ? D / 16 : D / 8;  // 16-byte chunks of a cached row
+        for (int32_t r = blockIdx.x; r < p.num_reqs; r += gridDim.x) {
+            const int32_t q0 = __ldg(p.cqsl + r), q1 = __ldg(p.cqsl + r + 1);
+            if (q1 - q0 != 1) {
+                if (lane == 0) set_err(p.err, YOCO_DEVERR_OFFSETS);
+                continue;
+            }
+            const int32_t pos = __ldg(p.seq_lens + r) - 1;
+            if (pos < 0 || pos / BS >= p.max_blocks) {
+                if (lane == 0) set_err(p.err, YOCO_DEVERR_POS_RANGE);
+                continue;
+            }
+            const int32_t blk = __ldg(p.block_table + static_cast<int64_t>(r) * p.max_blocks + pos / BS);
+            if (blk < 0 || blk >= p.num_blocks) {
+                if (lane == 0) set_err(p.err, YOCO_DEVERR_PAGE_RANGE);
+                continue;
+            }
+            for (int32_t h = 0; h < p.H_kv; ++h) {
+                const int64_t row = (static_cast<int64_t>(blk) * p.H_kv + h) * BS + pos % BS;
+                const uint4* ks = static_cast<const uint4*>(p.k_new) + (static_cast<int64_t>(q0) * p.H_kv + h) * (D / 8);
+                const uint4* vs = static_cast<const uint4*>(p.v_new) + (static_cast<int64_t>(q0) * p.H_kv + h) * (D / 8);
+                uint4* kd = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.k_pool) + row * D * S::ESZ);
+                uint4* vd = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.v_pool) + row * D * S::ESZ);
+                if constexpr (F8) {
+                    const float4 sc = __ldg(p.scales + static_cast<int64_t>(blk) * p.H_kv + h);
+                    if (!scale_usable(sc.x) || !scale_usable(sc.y)) {
+                        if (lane == 0) set_err(p.err, YOCO_DEVERR_SCALE);
+                        continue;
+                    }
+                    if (lane < CH) {
+                        const uint2 k0 = quantise8_e4m3(__ldg(ks + 2 * lane), sc.x);
+                        const uint2 k1 = quantise8_e4m3(__ldg(ks + 2 * lane + 1), sc.x);
+                        const uint2 v0 = quantise8_e4m3(__ldg(vs + 2 * lane), sc.y);
+                        const uint2 v1 = quantise8_e4m3(__ldg(vs + 2 * lane + 1), sc.y);
+                        kd[lane] = make_uint4(k0.x, k0.y, k1.x, k1.y);
+                        vd[lane] = make_uint4(v0.x, v0.y, v1.x, v1.y);
+                    }
+                } else if (lane < CH) {
+                    kd[lane] = __ldg(ks + lane);
+                    vd[lane] = __ldg(vs + lane);
+                }
+            }
+        }
+    }
     if (warp == NW - 1) {
         // rows with no key to attend: zero output, flag (requests spread over the CTAs)
         __nv_bfloat16* const outz = static_cast<__nv_bfloat16*>(p.out);
@@ -465,6 +514,24 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
         }
     };
     reset_state();
+    // Fused decode step: this lane's 16-byte chunk(s) of the segment's new token
+    // row (the request's one new token), K and V, loaded when the segment starts.
+    constexpr int PCH = F8 ? D / 16 : D / 8;  // 16-byte chunks of one cached token row
+    constexpr int PIN = F8 ? 2 : 1;           // bf16 input words per chunk
+    uint4 pk[PIN], pv[PIN];
+    constexpr bool fused = FUSE;
+    auto load_patch = [&](int32_t req, int32_t g) {
+        const int64_t tok = __ldg(p.cqsl + req + 1) - 1;
+        const uint4* kr = static_cast<const uint4*>(p.k_new) + (tok * p.H_kv + g) * (D / 8);
+        const uint4* vr_ = static_cast<const uint4*>(p.v_new) + (tok * p.H_kv + g) * (D / 8);
+        if (lane < PCH) {
+#pragma unroll
+            for (int u = 0; u < PIN; ++u) {
+                pk[u] = __ldg(kr + lane * PIN + u);
+                pv[u] = __ldg(vr_ + lane * PIN + u);
+            }
+        }
+    };
     // head dim of accumulator row gl (half 0) / gl + 8 (half 1) of 16-wide step md
     auto drow = [&](int md, int half) {
         return F8 ? md * 16 + 2 * gl + half : md * 16 + gl + 8 * half;
@@ -477,7 +544,10 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
     const int piece_bytes = (p.G * (D * 4 + 8) + 15) & ~15;
 
     for (int i = 0; i < n_my; ++i) {
-        if (i == 0 || cc.pp == (rev ? cc.pages - 1 : 0)) load_q(cc.n, cc.g);
+        if (i == 0 || cc.pp == (rev ? cc.pages - 1 : 0)) {
+            load_q(cc.n, cc.g);
+            if (fused) load_patch(cc.req, cc.g);
+        }
         const int st = i % STAGES;
         if (!mbar_wait_bounded(wbar + st, (i / STAGES) & 1, kWaitLimitNs)) {
             aborted = true;
@@ -513,6 +583,32 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
                     vinv = 1.f / sc4.y;
                     vr = 1.f;
                 }
+            }
+            if (fused && cc.pp == (cc.kv_len - 1) / BS) {
+                // Fused decode step: the row's newest key is this step's token, which
+                // this launch also appends to the pools; whatever the page copy
+                // brought for that slot, take it from the input (quantised by the
+                // append's rule for e4m3).
+                const int s = (cc.kv_len - 1) % BS;
+                uint8_t* kd = wbuf + st * S::STAGE_BYTES;
+                if (lane < PCH) {
+                    uint4 kw, vw;
+                    if constexpr (F8) {
+                        const float4 sc4 = stage_scale[warp * STAGES + st];
+                        const uint2 k0 = quantise8_e4m3(pk[0], sc4.x), k1 = quantise8_e4m3(pk[PIN - 1], sc4.x);
+                        const uint2 v0 = quantise8_e4m3(pv[0], sc4.y), v1 = quantise8_e4m3(pv[PIN - 1], sc4.y);
+                        kw = make_uint4(k0.x, k0.y, k1.x, k1.y);
+                        vw = make_uint4(v0.x, v0.y, v1.x, v1.y);
+                    } else {
+                        kw = pk[0];
+                        vw = pv[0];
+                    }
+                    const uint32_t off = swz<BS>(lane >> 3, s, lane & 7);
+                    *reinterpret_cast<uint4*>(kd + off) = kw;
+                    *reinterpret_cast<uint4*>(kd + S::PAGE_BYTES + off) = vw;
+                }
+                fence_proxy_async_smem();  // before a later copy refills the stage
+                __syncwarp();
             }
             if (nvalid < BS) {
                 // Rows past the causal end may hold stale data (even NaN), and a
@@ -1080,10 +1176,13 @@ template <int D, int BS, int NT, bool F8>
 cudaError_t launch_one(const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p, int sms,
                        cudaStream_t s) {
     using S = TcShape<D, BS, F8, NT>;
-    static unsigned long long smem_fwd = 0, smem_rev = 0;  // one flag word per kernel
-    auto kernel = p.reverse ? attn_tc_persistent<D, BS, NT, true, F8>
-                            : attn_tc_persistent<D, BS, NT, false, F8>;
-    cudaError_t e = ensure_smem_attr(kernel, S::SMEM, p.reverse ? smem_rev : smem_fwd);
+    static unsigned long long smem_fwd = 0, smem_rev = 0, smem_fuse = 0;  // one per kernel
+    const bool fuse = p.k_new != nullptr;
+    auto kernel = fuse ? attn_tc_persistent<D, BS, NT, false, F8, true>
+                       : (p.reverse ? attn_tc_persistent<D, BS, NT, true, F8, false>
+                                    : attn_tc_persistent<D, BS, NT, false, F8, false>);
+    cudaError_t e = ensure_smem_attr(kernel, S::SMEM,
+                                     fuse ? smem_fuse : (p.reverse ? smem_rev : smem_fwd));
     if (e != cudaSuccess) return e;
     const int ctas = tc_ctas(sms);
     AttnParams q = p;  // workspace: outputs of all pieces, then their (m, l), then headers

@@ -221,6 +221,29 @@ __device__ __forceinline__ uint32_t e4m3x2_hi_to_f16x2(uint32_t x) {
     return r;
 }
 
+// Scale records of the 8-bit cache: {k_scale, v_scale, -, -} per (page, kv head).
+__device__ __forceinline__ bool scale_usable(float s) { return s > 0.f && s <= 3.4e38f; }
+
+// Two floats -> two e4m3 codes (nearest, ties to even, saturating to +-448);
+// `lo` in bits 0..7.
+__device__ __forceinline__ uint32_t e4m3x2_rn_sat(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Eight bf16 values (two packed words each in a, b) -> eight e4m3 codes of
+// value / scale (float32 division, the cache's quantisation rule), low byte first.
+__device__ __forceinline__ uint2 quantise8_e4m3(uint4 a, float scale) {
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+    uint32_t c[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        c[i] = e4m3x2_rn_sat(__fdiv_rn(__uint_as_float(w[i] << 16), scale),
+                             __fdiv_rn(__uint_as_float(w[i] & 0xFFFF0000u), scale));
+    return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+}
+
 // 2^x with the hardware approximation (the softmax runs in the log2 domain).
 __device__ __forceinline__ float exp2_approx(float x) {
     float y;

@@ -170,7 +170,8 @@ yoco_status_t run_attn(const void* q, const void* k_cache, const void* v_cache,
                        int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
                        int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale,
                        yoco_dtype_t dtype, uint32_t flags, void* workspace,
-                       size_t workspace_bytes, int32_t* err_word, void* stream) {
+                       size_t workspace_bytes, int32_t* err_word, void* stream,
+                       const void* k_new = nullptr, const void* v_new = nullptr) {
     const bool e4m3 = dtype == YOCO_E4M3;
     if (flags & ~static_cast<uint32_t>(YOCO_ATTN_REVERSE | YOCO_ATTN_OVERLAP))
         return YOCO_ERR_INVALID_ARG;
@@ -206,6 +207,10 @@ yoco_status_t run_attn(const void* q, const void* k_cache, const void* v_cache,
     p.block_table = block_table;
     p.seq_lens = seq_lens;
     p.cqsl = cross_query_start_loc;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.k_pool = const_cast<void*>(k_cache);
+    p.v_pool = const_cast<void*>(v_cache);
     p.err = err_word;
     p.max_blocks = max_blocks_per_req;
     p.num_reqs = num_reqs;
@@ -274,4 +279,25 @@ extern "C" yoco_status_t yoco_cross_attn_paged_e4m3(
                           seq_lens, cross_query_start_loc, num_reqs, max_rows, max_seq_len,
                           num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
                           YOCO_E4M3, flags, workspace, workspace_bytes, err_word, stream);
+}
+
+extern "C" yoco_status_t yoco_cross_decode_step(
+    const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+    const float* page_scales, void* out, const int32_t* block_table, int32_t max_blocks_per_req,
+    const int32_t* seq_lens, const int32_t* query_start_loc, int32_t num_reqs,
+    int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+    int32_t block_size, int32_t num_blocks, float scale, yoco_dtype_t dtype, uint32_t flags,
+    void* workspace, size_t workspace_bytes, int32_t* err_word, void* stream) {
+    using namespace yoco;
+    if (dtype != YOCO_BF16 && dtype != YOCO_E4M3) return YOCO_ERR_UNSUPPORTED;
+    if (num_reqs > 0 && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)))
+        return YOCO_ERR_INVALID_ARG;
+    if (flags & YOCO_ATTN_REVERSE) return YOCO_ERR_INVALID_ARG;  // the fused step walks forward
+    // decode: one new token and one cross row per request, so query_start_loc is
+    // also the cross query_start_loc and num_reqs bounds the rows
+    return run_attn(q, k_cache, v_cache, dtype == YOCO_E4M3 ? page_scales : nullptr, out,
+                    block_table, max_blocks_per_req, seq_lens, query_start_loc, num_reqs,
+                    num_reqs, max_seq_len, num_q_heads, num_kv_heads, head_dim, block_size,
+                    num_blocks, scale, dtype, flags, workspace, workspace_bytes, err_word, stream,
+                    k_new, v_new);
 }

@@ -99,17 +99,6 @@ cudaError_t launch_append(const void* k_new, const void* v_new, void* k_cache, v
 
 // ---------------------------------------------------------------- e4m3 cache
 
-// Scale records of the 8-bit cache: {k_scale, v_scale, -, -} per (page, kv head).
-__device__ __forceinline__ bool scale_usable(float s) { return s > 0.f && s <= 3.4e38f; }
-
-// Two floats -> two e4m3 codes (nearest, ties to even, saturating to +-448);
-// `lo` in bits 0..7.
-__device__ __forceinline__ uint32_t e4m3x2_rn_sat(float lo, float hi) {
-    uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
 // Same row walk as kv_append_kernel; each lane quantises D / 32 consecutive
 // elements of K and of V (value / scale in float32, then the nearest code).
 template <int D>

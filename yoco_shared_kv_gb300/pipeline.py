@@ -147,7 +147,7 @@ class DeviceWorkload:
                                  ds.num_rows, self.err, stream)
 
     def attend(self, ds: DeviceStep, layer: int, stream=None, q: Optional[torch.Tensor] = None,
-               out: Optional[torch.Tensor] = None) -> None:
+               out: Optional[torch.Tensor] = None, cq: Optional[torch.Tensor] = None) -> None:
         """One cross-decoder layer. Odd layers walk the pages last to first, so each
         layer starts on what the previous one left in L2 (when `alternate` is on).
         Layers after the first overlap their start with the previous layer's end:
@@ -161,13 +161,34 @@ class DeviceWorkload:
         if self.e4m3:
             N.yoco_cross_attn_paged_e4m3(
                 d["q"][layer] if q is None else q, self.k_cache, self.v_cache, self.page_scales,
-                ds.out[layer] if out is None else out, d["block_table"], d["seq_lens"], ds.cqsl,
-                ds.max_seq_len, self.wl.scale, ds.workspace, self.err, stream, flags=flags)
+                ds.out[layer] if out is None else out, d["block_table"], d["seq_lens"],
+                ds.cqsl if cq is None else cq, ds.max_seq_len, self.wl.scale, ds.workspace,
+                self.err, stream, flags=flags)
             return
         N.yoco_cross_attn_paged(d["q"][layer] if q is None else q, self.k_cache, self.v_cache,
                                 ds.out[layer] if out is None else out, d["block_table"],
-                                d["seq_lens"], ds.cqsl, ds.max_seq_len, self.wl.scale,
-                                ds.workspace, self.err, stream, flags=flags)
+                                d["seq_lens"], ds.cqsl if cq is None else cq, ds.max_seq_len,
+                                self.wl.scale, ds.workspace, self.err, stream, flags=flags)
+
+    def decode_only(self, i: int) -> bool:
+        """Every request of step i schedules one token and gets one cross row."""
+        st = self.steps[i].step
+        qsl = np.asarray(st.query_start_loc)
+        rpr = st.rows_per_req
+        return bool((np.diff(qsl) == 1).all() and (rpr is None or (np.asarray(rpr) == 1).all())
+                    and self.wl.dtype == "bf16")
+
+    def fused_step(self, i: int, stream=None, layers: Optional[int] = None) -> None:
+        """A decode step with the append fused into layer 0 (yoco_cross_decode_step),
+        then every later layer; the row selection is the identity for decode."""
+        ds = self.steps[i]
+        d = ds.dev
+        N.yoco_cross_decode_step(d["q"][0], d["k_new"], d["v_new"], self.k_cache, self.v_cache,
+                                 self.page_scales, ds.out[0], d["block_table"], d["seq_lens"],
+                                 d["qsl"], ds.max_seq_len, self.wl.scale, ds.workspace, self.err,
+                                 stream)
+        for layer in range(1, self.wl.layers if layers is None else layers):
+            self.attend(ds, layer, stream, cq=d["qsl"])
 
     def run_fill(self, stream=None) -> None:
         if self.fill is not None:
