@@ -56,3 +56,56 @@ def test_full_size(P, idx):
     dw.attend(ds, 0, out=again)
     torch.cuda.synchronize()
     assert torch.equal(again.view(torch.int16), ds.out[0].view(torch.int16))
+
+
+@pytest.mark.parametrize("idx", [1, 2, 3, 4])
+def test_full_size_e4m3(P, idx):
+    """The e4m3 cache at full size: quantising append bit-exact over the whole pools,
+    attention on sampled rows x layers against the oracle over the dequantised cache."""
+    from tests.helpers import oracle_e4m3_pools, oracle_e4m3_step_out
+    from workloads import page_scales
+    wl = FULL[idx]()
+    sc = page_scales(wl)
+    dw = P.DeviceWorkload(wl, kv="e4m3", page_scales=sc)
+    dw.run_fill()
+    dw.run_step(0)
+    torch.cuda.synchronize()
+    assert dw.error_bits() == 0
+    step = wl.steps[0]
+    ds = dw.steps[0]
+    kp, vp = oracle_e4m3_pools(wl, sc)
+    assert np.array_equal(dw.k_cache.cpu().numpy(), kp)
+    assert np.array_equal(dw.v_cache.cpu().numpy(), vp)
+    got = gpu_out(ds.out)
+    assert np.isfinite(got).all()
+    n = step.rows_upper
+    rng = np.random.default_rng(100 + idx)
+    rows = sorted(set([0, n - 1] + rng.choice(n, size=min(n, 3), replace=False).tolist()))
+    layers = [0, wl.layers - 1]
+    ref = oracle_e4m3_step_out(wl, step, kp, vp, sc, layers=layers, rows=rows)
+    err = np.abs(got[layers][:, rows] - ref).max()
+    assert err <= ATOL["bf16"], (wl.name, err)
+    again = torch.empty_like(ds.out[1])
+    dw.attend(ds, 1, out=again)  # an odd layer: the reverse page walk at this size
+    torch.cuda.synchronize()
+    assert torch.equal(again.view(torch.int16), ds.out[1].view(torch.int16))
+
+
+@pytest.mark.parametrize("kv", ["native", "e4m3"])
+def test_full_size_fused_decode_step(P, kv):
+    """Pure decode at full size: the fused step leaves the same cache and the same
+    outputs, bit for bit, as the separate append, selection and attention."""
+    from workloads import page_scales
+    wl = FULL[1]()
+    sc = page_scales(wl) if kv == "e4m3" else None
+    a = P.DeviceWorkload(wl, kv=kv, page_scales=sc)
+    b = P.DeviceWorkload(wl, kv=kv, page_scales=sc)
+    for dw in (a, b):
+        dw.run_fill()
+    a.run_step(0)
+    b.fused_step(0)
+    torch.cuda.synchronize()
+    assert a.error_bits() == 0 and b.error_bits() == 0
+    assert torch.equal(a.k_cache.view(torch.uint8), b.k_cache.view(torch.uint8))
+    assert torch.equal(a.v_cache.view(torch.uint8), b.v_cache.view(torch.uint8))
+    assert torch.equal(a.steps[0].out.view(torch.int16), b.steps[0].out.view(torch.int16))
