@@ -34,6 +34,12 @@ def _nvcc() -> str:
 def _stale() -> bool:
     if not os.path.exists(LIB):
         return True
+    try:
+        if open(LIB + ".defines").read() != os.environ.get("YOCO_NVCC_DEFINES", ""):
+            return True
+    except OSError:
+        if os.environ.get("YOCO_NVCC_DEFINES", ""):
+            return True
     t = os.path.getmtime(LIB)
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + \
            [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)] + [os.path.abspath(__file__)]
@@ -48,7 +54,9 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     def compile_one(src):
         obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
-        cmd = [nvcc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        # YOCO_NVCC_DEFINES: extra -D tunables (e.g. "-DYOCO_TC_F8_NW=4") for sweeps
+        extra = os.environ.get("YOCO_NVCC_DEFINES", "").split()
+        cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd += ["-Xptxas", "-v"]
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -66,6 +74,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(LIB + ".defines", "w") as f:
+        f.write(os.environ.get("YOCO_NVCC_DEFINES", ""))
     return LIB
 
 

@@ -47,6 +47,14 @@ namespace {
 #ifndef YOCO_TC_ST16
 #define YOCO_TC_ST16 3
 #endif
+// e4m3 cache: warps per CTA and shared-memory bytes of the warps' rings
+// (0 = derived from the piece sizes, below)
+#ifndef YOCO_TC_F8_NW
+#define YOCO_TC_F8_NW 0
+#endif
+#ifndef YOCO_TC_F8_RING
+#define YOCO_TC_F8_RING 196608
+#endif
 
 // F8: the cache holds e4m3 bytes (one byte per element) instead of bf16.
 // NT: 8-head tiles of the group (1 for groups up to 8, else 2).
@@ -57,19 +65,26 @@ struct TcShape {
     static constexpr int STAGE_BYTES = 2 * PAGE_BYTES;    // K + V
     // a warp's two end-of-slice pieces at the largest group of this NT
     static constexpr int PIECE_PAIR = 2 * (8 * NT * (D * 4 + 8) + 16);
+    // the most warps (8, 4, 2) whose ring share holds two stages and the two pieces
+    static constexpr int F8_FITS8 =
+        PIECE_PAIR <= YOCO_TC_F8_RING / 8 && 2 * STAGE_BYTES <= YOCO_TC_F8_RING / 8;
+    static constexpr int F8_FITS4 =
+        PIECE_PAIR <= YOCO_TC_F8_RING / 4 && 2 * STAGE_BYTES <= YOCO_TC_F8_RING / 4;
+    static constexpr int F8_NW =
+        YOCO_TC_F8_NW > 0 ? YOCO_TC_F8_NW : (F8_FITS8 ? 8 : (F8_FITS4 ? 4 : 2));
     static constexpr int NW =
-        F8 ? (PIECE_PAIR <= 24576 ? 8 : 4)
-           : (STAGE_BYTES <= 8192 ? 8 : (STAGE_BYTES <= 16384 ? YOCO_TC_NW16 : 2));
+        F8 ? F8_NW : (STAGE_BYTES <= 8192 ? 8 : (STAGE_BYTES <= 16384 ? YOCO_TC_NW16 : 2));
     // e4m3 pages are small: deepen the ring to keep ~192 KiB in flight per SM
+    static constexpr int F8_STAGES = YOCO_TC_F8_RING / F8_NW / STAGE_BYTES;
     static constexpr int STAGES =
-        F8 ? (196608 / NW / STAGE_BYTES < 3 ? 3 : 196608 / NW / STAGE_BYTES)
-           : (STAGE_BYTES == 16384 ? YOCO_TC_ST16 : 3);
+        F8 ? (F8_STAGES < 2 ? 2 : F8_STAGES) : (STAGE_BYTES == 16384 ? YOCO_TC_ST16 : 3);
     static constexpr int SUBE = 128 / ESZ;  // elements per 128-byte row of a sub-tile
     static constexpr int KSUB = D / SUBE;   // 128-byte swizzled sub-tiles per row
     static constexpr int SUB_BYTES = BS * 128;
     static constexpr int MT = BS / 16;   // 16-token tiles per page
     static constexpr int KD = D / 16;    // 16-wide steps along head_dim
     static constexpr int SMEM = NW * STAGES * STAGE_BYTES + 1024;
+    static_assert(SMEM <= 200 * 1024, "the rings must leave room for static shared memory");
 };
 
 // Byte offset of (token t, 16-byte chunk j of head-dim sub-tile c) in a
