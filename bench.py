@@ -54,6 +54,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-cold", action="store_true", help="skip the cold-L2 single-layer timing")
     ap.add_argument("--seed-offset", type=int, default=0)
     ap.add_argument("--kv", choices=["native", "e4m3"], default="native",
                     help="cache format: the workload's dtype, or e4m3 with per-page scales")
@@ -331,6 +332,32 @@ def run_ours(args, rank, world, local):
         a1.record(stream)
     stream.synchronize()
     attn_launch_ms = a0.elapsed_time(a1) / (reps * L)
+    # one layer from a cold L2: a graph of (flush, layer 0) minus a graph of the flush alone
+    cold_ms = None
+    if not args.no_cold:
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+        g_fl, g_cold = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_fl, stream=stream):
+            flush.zero_()
+        with torch.cuda.graph(g_cold, stream=stream):
+            flush.zero_()
+            dw.attend(ds, 0)
+        times = []
+        for g in (g_fl, g_cold):
+            c0 = torch.cuda.Event(enable_timing=True)
+            c1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    g.replay()
+                c0.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                c1.record(stream)
+            stream.synchronize()
+            times.append(c0.elapsed_time(c1) / reps)
+        cold_ms = max(times[1] - times[0], 1e-6)
+        del flush
 
     max_ms, total_kv_bytes, total_rows = aggregate_ranks(
         elapsed_ms, acc["kv_bytes_step"] * args.steps, acc["rows"] * L * args.steps, world, dev)
@@ -402,6 +429,11 @@ def run_ours(args, rank, world, local):
                      "launch_ms": round(attn_launch_ms, 5), "peak_source": peaks["source"]},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
+        "per_layer_cold_l2": None if cold_ms is None else {
+            "launch_ms": round(cold_ms, 5),
+            "achieved_gbs": round(acc["attn_bytes_layer"] / (cold_ms / 1e3) / 1e9, 2),
+            "frac": round(acc["attn_bytes_layer"] / (cold_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+            "how": "graph(flush 2 x L2 with a memset, layer 0) minus graph(flush), CUDA events"},
     }
     if e2e is not None:
         res["e2e"] = e2e
