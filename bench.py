@@ -265,10 +265,13 @@ def run_ours(args, rank, world, local):
         raise SystemExit("--fused needs a decode-only workload (one token and one row per request)")
 
     def step_fn(i):
+        step_fn_on(dw.steps[i])
+
+    def step_fn_on(d_s):
         if args.fused:
-            dw.fused_step(i)
+            dw.fused_step_on(d_s)
         else:
-            dw.run_step(i)
+            dw.run_step_on(d_s)
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
         dw.run_fill(stream)
@@ -365,28 +368,59 @@ def run_ours(args, rank, world, local):
     if dw.error_bits() != 0:
         raise RuntimeError(f"device error bits {dw.error_bits():#x}")
 
-    # end to end through the C ABI: pinned host inputs -> device, step, outputs -> host
+    # End to end through the C ABI: every step copies its inputs from pinned host
+    # memory and reads its outputs back, as a serving loop does. Two buffer sets
+    # alternate, so the copies of one step overlap the computation of another
+    # (copy-in stream, compute stream, read-back stream, ordered by events); the
+    # timed region covers every copy.
     e2e = None
     if not args.no_e2e:
-        out_host = torch.empty(ds.out.shape, dtype=ds.out.dtype, pin_memory=True)
+        ds_b = dw.step_buffers(step_i)
+        g_b = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            step_fn_on(ds_b)  # eager once, then capture
+        stream.synchronize()
+        with torch.cuda.graph(g_b, stream=stream):
+            step_fn_on(ds_b)
+        bufs = [(ds, g_step), (ds_b, g_b)]
+        out_host = [torch.empty(b.out.shape, dtype=b.out.dtype, pin_memory=True) for b, _ in bufs]
+        s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        ev_in = [torch.cuda.Event() for _ in bufs]
+        ev_done = [torch.cuda.Event() for _ in bufs]
+        ev_read = [torch.cuda.Event() for _ in bufs]
+        k_e2e = max(1, min(args.steps, 200))
+        warm = 4
+        h2d = d2h = 0
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        k_e2e = max(1, min(args.steps, 200))
-        h2d = d2h = 0
-        with torch.cuda.stream(stream):
-            for _ in range(3):
-                ds.h2d(stream)
-                g_step.replay()
-                out_host.copy_(ds.out, non_blocking=True)
-            stream.synchronize()
-            e0.record(stream)
-            for _ in range(k_e2e):
-                h2d = ds.h2d(stream)
-                g_step.replay()
-                out_host.copy_(ds.out, non_blocking=True)
-                d2h = out_host.numel() * out_host.element_size()
-            e1.record(stream)
-        stream.synchronize()
+        torch.cuda.synchronize(dev)
+        for k in range(warm + k_e2e):
+            if k == warm:
+                torch.cuda.synchronize(dev)
+                e0.record(stream)
+                s_in.wait_event(e0)
+                s_out.wait_event(e0)
+            j = k % 2
+            dsj, gj = bufs[j]
+            if k >= 2:
+                s_in.wait_event(ev_done[j])   # the step two back has read these inputs
+            with torch.cuda.stream(s_in):
+                h2d = dsj.h2d(s_in)
+                ev_in[j].record(s_in)
+            stream.wait_event(ev_in[j])
+            if k >= 2:
+                stream.wait_event(ev_read[j])  # and its outputs have been read back
+            with torch.cuda.stream(stream):
+                gj.replay()
+                ev_done[j].record(stream)
+            s_out.wait_event(ev_done[j])
+            with torch.cuda.stream(s_out):
+                out_host[j].copy_(dsj.out, non_blocking=True)
+                ev_read[j].record(s_out)
+            d2h = out_host[j].numel() * out_host[j].element_size()
+        stream.wait_event(ev_read[(warm + k_e2e - 1) % 2])
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
         e2e_ms = e0.elapsed_time(e1) / k_e2e
         if world > 1:
             import torch.distributed as dist
@@ -395,7 +429,8 @@ def run_ours(args, rank, world, local):
             e2e_ms = float(t[0])
         e2e = {"value": round(total_kv_bytes / args.steps / (e2e_ms / 1e3) / 1e9, 3), "unit": "GB/s",
                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h)}
+               "d2h_bytes_per_step": int(d2h),
+               "how": "two input/output buffer sets; copies overlap the other set's step"}
 
     ms_per_step = max_ms / args.steps
     value = total_kv_bytes / (max_ms / 1e3) / 1e9

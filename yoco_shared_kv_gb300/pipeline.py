@@ -178,10 +178,17 @@ class DeviceWorkload:
         return bool((np.diff(qsl) == 1).all() and (rpr is None or (np.asarray(rpr) == 1).all())
                     and self.wl.dtype == "bf16")
 
+    def step_buffers(self, i: int, pin_host: bool = True) -> DeviceStep:
+        """Another set of device buffers (inputs, outputs, scratch) for step i, so that
+        one set's inputs can be copied in while a step runs on the other."""
+        return DeviceStep(self.wl, self.wl.steps[i], self.device, pin_host, self.e4m3)
+
     def fused_step(self, i: int, stream=None, layers: Optional[int] = None) -> None:
+        self.fused_step_on(self.steps[i], stream, layers)
+
+    def fused_step_on(self, ds: DeviceStep, stream=None, layers: Optional[int] = None) -> None:
         """A decode step with the append fused into layer 0 (yoco_cross_decode_step),
         then every later layer; the row selection is the identity for decode."""
-        ds = self.steps[i]
         d = ds.dev
         N.yoco_cross_decode_step(d["q"][0], d["k_new"], d["v_new"], self.k_cache, self.v_cache,
                                  self.page_scales, ds.out[0], d["block_table"], d["seq_lens"],
@@ -195,8 +202,10 @@ class DeviceWorkload:
             self.append(self.fill, stream)
 
     def run_step(self, i: int, stream=None, layers: Optional[int] = None) -> None:
+        self.run_step_on(self.steps[i], stream, layers)
+
+    def run_step_on(self, ds: DeviceStep, stream=None, layers: Optional[int] = None) -> None:
         """append -> select -> every cross-decoder layer, all enqueued on one stream."""
-        ds = self.steps[i]
         self.append(ds, stream)
         self.select(ds, stream)
         for layer in range(self.wl.layers if layers is None else layers):
