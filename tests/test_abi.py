@@ -141,3 +141,26 @@ def test_e4m3_workspace_and_traffic(lib_path):
     pages = 7
     assert tb == 100 * 2 * 2 * 128 * 2 + 2 * 8 * 128 * 2 + 4 * pages * 2
     assert t8 == 100 * 2 * 2 * 128 * 1 + 2 * 8 * 128 * 2 + 20 * pages * 2
+
+
+def test_fused_step_host_validation(lib_path):
+    from yoco_shared_kv_gb300 import _native as N
+    L = N.lib
+    fake = 1 << 20  # never dereferenced: every call below returns before a launch
+
+    def step(**kw):
+        a = dict(kn=fake, dt=N.YOCO_BF16, flags=0, d=256)
+        a.update(kw)
+        return L.yoco_cross_decode_step(fake, a["kn"], fake, fake, fake, fake, fake, fake, 4,
+                                        fake, fake, 1, 64, 8, 2, a["d"], 16, 100, 0.0625, a["dt"],
+                                        a["flags"], None, 0, None, None)
+    assert step(flags=N.YOCO_ATTN_REVERSE) == N.YOCO_ERR_INVALID_ARG  # the step walks forward
+    assert step(dt=N.YOCO_F32) == N.YOCO_ERR_UNSUPPORTED
+    assert step(kn=None) == N.YOCO_ERR_INVALID_ARG
+    assert step(kn=fake + 8) == N.YOCO_ERR_INVALID_ARG
+    assert step(d=96) == N.YOCO_ERR_UNSUPPORTED
+    assert step() == N.YOCO_ERR_WORKSPACE  # every check passed, no workspace given
+    # the allocation-free entry does not take the e4m3 cache
+    assert L.yoco_cross_attn_paged_noalloc(fake, fake, fake, fake, fake, 4, fake, fake, 1, 1, 64,
+                                           8, 2, 256, 16, 100, 0.0625, N.YOCO_E4M3, None,
+                                           None) == N.YOCO_ERR_UNSUPPORTED

@@ -160,3 +160,53 @@ def test_e4m3_append_tie_and_bad_scale(P, N):
                                  D ** -0.5, ws, err)
     torch.cuda.synchronize()
     assert int(err.item()) & N.DEVERR_SCALE
+
+
+def test_e4m3_empty_row_and_bad_page_flagged(P, N):
+    wl = SMALL[1]()
+    scales = page_scales(wl)
+    dw = _run(P, wl, scales)
+    ds = dw.steps[0]
+    d = ds.dev
+    sc = dw.page_scales
+    # seq_len 0 for request 0: its row has no key -> zero output + flag
+    sl = d["seq_lens"].clone()
+    sl[0] = 0
+    out = torch.full_like(ds.out[0], 3.0)
+    dw.err.zero_()
+    N.yoco_cross_attn_paged_e4m3(d["q"][0], dw.k_cache, dw.v_cache, sc, out, d["block_table"], sl,
+                                 ds.cqsl, ds.max_seq_len, wl.scale, ds.workspace, dw.err)
+    torch.cuda.synchronize()
+    assert dw.error_bits() & N.DEVERR_EMPTY_ROW
+    assert (out[0] == 0).all()
+    # a page id past the pool: flagged, skipped, no fault
+    bt = d["block_table"].clone()
+    bt[3, 2] = -4
+    dw.err.zero_()
+    N.yoco_cross_attn_paged_e4m3(d["q"][0], dw.k_cache, dw.v_cache, sc, out, bt, d["seq_lens"],
+                                 ds.cqsl, ds.max_seq_len, wl.scale, ds.workspace, dw.err)
+    torch.cuda.synchronize()
+    assert dw.error_bits() & N.DEVERR_PAGE_RANGE
+
+
+@pytest.mark.parametrize("kv", ["native", "e4m3"])
+def test_fused_step_bad_page_flagged(P, N, kv):
+    wl = SMALL[1]()
+    sc = page_scales(wl) if kv == "e4m3" else None
+    dw = P.DeviceWorkload(wl, kv=kv, page_scales=sc)
+    dw.run_fill()
+    ds = dw.steps[0]
+    d = ds.dev
+    bt = d["block_table"].clone()
+    r = 2
+    last_page = (int(wl.steps[0].seq_lens[r]) - 1) // wl.block_size
+    bt[r, last_page] = wl.num_blocks + 5  # the new token's page is out of the pool
+    before = dw.k_cache.clone()
+    N.yoco_cross_decode_step(d["q"][0], d["k_new"], d["v_new"], dw.k_cache, dw.v_cache,
+                             dw.page_scales, ds.out[0], bt, d["seq_lens"], d["qsl"],
+                             ds.max_seq_len, wl.scale, ds.workspace, dw.err)
+    torch.cuda.synchronize()
+    assert dw.error_bits() & N.DEVERR_PAGE_RANGE
+    # nothing was written for the skipped token; the other requests' tokens were
+    changed = (dw.k_cache.view(torch.uint8) != before.view(torch.uint8))
+    assert changed.any()

@@ -59,6 +59,8 @@ extern "C" yoco_status_t yoco_cross_attn_paged_noalloc(
     int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale,
     yoco_dtype_t dtype, int32_t* err_word, void* stream) {
     using namespace yoco;
+    // the e4m3 cache has its own entry; refuse it (and unknown dtypes) before any CUDA call
+    if (!dtype_ok(dtype)) return YOCO_ERR_UNSUPPORTED;
     const size_t need = yoco_cross_attn_workspace_size(max_rows, num_q_heads, num_kv_heads,
                                                        head_dim, block_size, max_seq_len, dtype);
     if (need > kStaticScratchBytes) return YOCO_ERR_WORKSPACE;  // more than the fixed array holds
