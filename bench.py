@@ -55,6 +55,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-cold", action="store_true", help="skip the cold-L2 single-layer timing")
+    ap.add_argument("--l2-window", action="store_true",
+                    help="keep part of the K pool persisting in L2 across layers (yoco_set_l2_window)")
+    ap.add_argument("--no-alternate", action="store_true",
+                    help="every layer walks its pages forward (no cross-layer L2 reuse by direction)")
     ap.add_argument("--seed-offset", type=int, default=0)
     ap.add_argument("--kv", choices=["native", "e4m3"], default="native",
                     help="cache format: the workload's dtype, or e4m3 with per-page scales")
@@ -257,6 +261,8 @@ def run_ours(args, rank, world, local):
                               page_scales=page_scales(wl))
     else:
         dw = P.DeviceWorkload(wl, dev, pin_host=not args.no_e2e, sentinel=False)
+    if args.no_alternate:
+        dw.alternate = False
     step_i = len(wl.steps) - 1
     ds = dw.steps[step_i]
     acc = accounting(wl, wl.steps[step_i], e4m3)
@@ -273,6 +279,9 @@ def run_ours(args, rank, world, local):
         else:
             dw.run_step_on(d_s)
     stream = torch.cuda.Stream(device=dev)
+    if args.l2_window:  # before capture: the kernel nodes take the stream's window
+        N.yoco_set_l2_window(dw.k_cache, dw.k_cache.numel() * dw.k_cache.element_size(), -1.0,
+                             stream=stream)
     with torch.cuda.stream(stream):
         dw.run_fill(stream)
         for i in range(step_i):  # earlier steps of a multi-step schedule

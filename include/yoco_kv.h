@@ -337,6 +337,10 @@ size_t yoco_cross_attn_noalloc_capacity(void);
  * set-aside is a property of this process's CUDA context only. Used to
  * keep a shared cache resident across the serial cross-decoder layers,
  * which re-read it one after another ("YOCO 论文与推理数据流详解" §11).
+ * The window is cut to the device's largest window; hit_ratio in [0, 1]
+ * is the fraction of its lines given the persisting property, and a
+ * negative hit_ratio means "as many as the set-aside holds" (set-aside /
+ * window), so that the same lines stay resident from one layer to the next.
  */
 yoco_status_t yoco_set_l2_window(void* stream, void* base, size_t bytes, float hit_ratio);
 

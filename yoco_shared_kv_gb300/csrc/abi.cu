@@ -47,7 +47,7 @@ extern "C" yoco_status_t yoco_set_l2_window(void* stream, void* base, size_t byt
         YOCO_CUDA_OK(cudaStreamSetAttribute(s, cudaStreamAttributeAccessPolicyWindow, &attr));
         return YOCO_OK;
     }
-    if (!(hit_ratio >= 0.f && hit_ratio <= 1.f)) return YOCO_ERR_INVALID_ARG;
+    if (!(hit_ratio <= 1.f)) return YOCO_ERR_INVALID_ARG;  // negative: automatic
     int dev = 0, max_win = 0, max_persist = 0;
     YOCO_CUDA_OK(cudaGetDevice(&dev));
     YOCO_CUDA_OK(cudaDeviceGetAttribute(&max_win, cudaDevAttrMaxAccessPolicyWindowSize, dev));
@@ -59,7 +59,10 @@ extern "C" yoco_status_t yoco_set_l2_window(void* stream, void* base, size_t byt
     YOCO_CUDA_OK(cudaDeviceSetLimit(cudaLimitPersistingL2CacheSize, keep));
     attr.accessPolicyWindow.base_ptr = base;
     attr.accessPolicyWindow.num_bytes = win;
-    attr.accessPolicyWindow.hitRatio = hit_ratio;
+    // automatic ratio: as many of the window's lines as the set-aside holds
+    attr.accessPolicyWindow.hitRatio =
+        hit_ratio < 0.f ? static_cast<float>(static_cast<double>(keep) / static_cast<double>(win))
+                        : hit_ratio;
     attr.accessPolicyWindow.hitProp = cudaAccessPropertyPersisting;
     attr.accessPolicyWindow.missProp = cudaAccessPropertyStreaming;
     YOCO_CUDA_OK(cudaStreamSetAttribute(s, cudaStreamAttributeAccessPolicyWindow, &attr));
