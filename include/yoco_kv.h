@@ -75,6 +75,7 @@ typedef enum { YOCO_F32 = 0, YOCO_BF16 = 1, YOCO_E4M3 = 2 } yoco_dtype_t;
 /* Flags of yoco_cross_attn_paged. */
 #define YOCO_ATTN_REVERSE 0x1u /* tensor-core paths: walk each worker's pages last to first */
 #define YOCO_ATTN_OVERLAP 0x2u /* tensor-core paths: may start while the previous kernel drains */
+#define YOCO_ATTN_KEEP_TAIL 0x4u /* tensor-core paths: L2 hints that keep this walk's tail for the next layer */
 
 /* Bits OR-ed into *err_word by device code. */
 #define YOCO_DEVERR_PAGE_RANGE 0x1   /* block_table entry outside [0, num_blocks) */
@@ -162,8 +163,8 @@ size_t yoco_cross_attn_workspace_size(int32_t max_rows, int32_t num_q_heads, int
  *   max_rows               host bound on the number of rows (grid size)
  *   max_seq_len            host bound on seq_lens (sizes the split-KV grid)
  *   scale                  softmax scale (1/sqrt(head_dim) for the pages' definition)
- *   flags                  bits of YOCO_ATTN_REVERSE | YOCO_ATTN_OVERLAP (other bits are
- *                          rejected; both are ignored on the fp32 path).
+ *   flags                  bits of YOCO_ATTN_REVERSE | YOCO_ATTN_OVERLAP | YOCO_ATTN_KEEP_TAIL
+ *                          (other bits are rejected; all are ignored on the fp32 path).
  *                          REVERSE: the serial layers re-read one cache ("YOCO 论文与推理
  *                          数据流详解" §11); with the flag set on every other layer, a layer
  *                          starts on the pages the previous one read last, which are still
@@ -174,6 +175,11 @@ size_t yoco_cross_attn_workspace_size(int32_t max_rows, int32_t num_q_heads, int
  *                          Set it only when that kernel writes none of those (for example
  *                          the previous cross-decoder layer); queries, outputs and the
  *                          workspace are touched only after that kernel has finished.
+ *                          KEEP_TAIL: the pages are copied with an L2 evict-first hint except
+ *                          the last ones each worker reads (evict-last, about 40 MB for a
+ *                          bf16/fp32 cache, 20 MB for e4m3), which stay in L2 for the next
+ *                          layer; meant for layers that alternate YOCO_ATTN_REVERSE over a
+ *                          cache larger than L2. Hints only: the result is unchanged.
  *   workspace              device scratch of >= yoco_cross_attn_workspace_size(...) bytes,
  *                          16-byte aligned; contents need no initialisation
  *   err_word               device int32 or NULL

@@ -74,7 +74,7 @@ def test_host_validation_rejects_before_launch(lib_path):
     assert call(hq=34, hkv=2) == 2  # group of 17
     assert call(dt=5) == 2          # unknown dtype
     assert call() == 1              # null pointers
-    assert call(flags=0x4) == 1     # unknown flag bit
+    assert call(flags=0x8) == 1     # unknown flag bit
     L.yoco_select_cross_rows.restype = ctypes.c_int
     L.yoco_select_cross_rows.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp]
     assert L.yoco_select_cross_rows(None, None, -1, None, None, None, None, None) == 1
@@ -110,7 +110,7 @@ def test_e4m3_host_validation(lib_path):
     assert attn(bs=8) == N.YOCO_ERR_UNSUPPORTED
     assert attn(sc=None) == N.YOCO_ERR_INVALID_ARG  # scale records are required
     assert attn(sc=fake + 8) == N.YOCO_ERR_INVALID_ARG  # 16-byte records, 16-byte aligned
-    assert attn(flags=0x4) == N.YOCO_ERR_INVALID_ARG
+    assert attn(flags=0x8) == N.YOCO_ERR_INVALID_ARG
     assert attn() == N.YOCO_ERR_WORKSPACE           # no workspace given
     # the bf16 entry refuses the e4m3 dtype
     assert L.yoco_cross_attn_paged(fake, fake, fake, fake, fake, 4, fake, fake, 1, 1, 64, 8, 2,

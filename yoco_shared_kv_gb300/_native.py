@@ -21,6 +21,7 @@ YOCO_OK, YOCO_ERR_INVALID_ARG, YOCO_ERR_UNSUPPORTED, YOCO_ERR_WORKSPACE, YOCO_ER
 YOCO_F32, YOCO_BF16, YOCO_E4M3 = 0, 1, 2
 YOCO_ATTN_REVERSE = 0x1
 YOCO_ATTN_OVERLAP = 0x2
+YOCO_ATTN_KEEP_TAIL = 0x4
 DEVERR_PAGE_RANGE = 0x1
 DEVERR_POS_RANGE = 0x2
 DEVERR_EMPTY_ROW = 0x4

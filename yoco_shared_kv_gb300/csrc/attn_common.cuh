@@ -34,6 +34,7 @@ struct AttnParams {
     float scale_log2;           // softmax scale * log2(e)
     int32_t reverse;            // tensor-core path: walk each worker's pages from the end
     int32_t overlap;            // tensor-core path: launch as a programmatic dependent
+    int32_t keep_tail;          // tensor-core path: L2 hints, keep this walk's tail for the next layer
 };
 
 // Wait limit for one asynchronous page copy before a kernel gives up.

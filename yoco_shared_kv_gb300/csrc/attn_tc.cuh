@@ -360,6 +360,16 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
         blk_next = __ldg(p.block_table + static_cast<int64_t>(pc.req) * p.max_blocks + pc.pp);
     };
 
+    // With keep_tail, the pages are streamed through L2 with an evict-first
+    // hint except the last keep_pages of this warp's walk (evict-last): about
+    // kKeepBytes over the grid stay in L2 for the next layer, which walks the
+    // other way and starts on them.
+    constexpr int64_t kKeepBytes = (F8 ? 20ll : 40ll) << 20;
+    const bool keep_tail = p.keep_tail != 0;
+    const uint64_t pol_keep = keep_tail ? make_l2_policy_evict_last() : 0;
+    const uint64_t pol_stream = keep_tail ? make_l2_policy_evict_first() : 0;
+    const int keep_pages = static_cast<int>(
+        kKeepBytes / (static_cast<int64_t>(gridDim.x) * NW * S::STAGE_BYTES));
     auto issue = [&](int i) {  // lane 0 only; pc is at page i, blk_next its entry
         const int st = i % STAGES;
         uint64_t* bar = wbar + st;
@@ -374,10 +384,19 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
             uint8_t* kd = wbuf + st * S::STAGE_BYTES;
             uint8_t* vd = kd + S::PAGE_BYTES;
             const int32_t y = (blk * p.H_kv + pc.g) * BS;
+            if (keep_tail) {
+                const uint64_t pol = i >= n_my - keep_pages ? pol_keep : pol_stream;
 #pragma unroll
-            for (int c = 0; c < S::KSUB; ++c) {
-                tma_load_2d(kd + c * S::SUB_BYTES, &tm_k, c * S::SUBE, y, bar);
-                tma_load_2d(vd + c * S::SUB_BYTES, &tm_v, c * S::SUBE, y, bar);
+                for (int c = 0; c < S::KSUB; ++c) {
+                    tma_load_2d_hint(kd + c * S::SUB_BYTES, &tm_k, c * S::SUBE, y, bar, pol);
+                    tma_load_2d_hint(vd + c * S::SUB_BYTES, &tm_v, c * S::SUBE, y, bar, pol);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < S::KSUB; ++c) {
+                    tma_load_2d(kd + c * S::SUB_BYTES, &tm_k, c * S::SUBE, y, bar);
+                    tma_load_2d(vd + c * S::SUB_BYTES, &tm_v, c * S::SUBE, y, bar);
+                }
             }
             if constexpr (F8)
                 bulk_load(&stage_scale[warp * STAGES + st],

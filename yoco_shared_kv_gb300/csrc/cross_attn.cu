@@ -173,7 +173,7 @@ yoco_status_t run_attn(const void* q, const void* k_cache, const void* v_cache,
                        size_t workspace_bytes, int32_t* err_word, void* stream,
                        const void* k_new = nullptr, const void* v_new = nullptr) {
     const bool e4m3 = dtype == YOCO_E4M3;
-    if (flags & ~static_cast<uint32_t>(YOCO_ATTN_REVERSE | YOCO_ATTN_OVERLAP))
+    if (flags & ~static_cast<uint32_t>(YOCO_ATTN_REVERSE | YOCO_ATTN_OVERLAP | YOCO_ATTN_KEEP_TAIL))
         return YOCO_ERR_INVALID_ARG;
     if (!(dtype_ok(dtype) || e4m3) || !head_dim_ok(head_dim) || !block_size_ok(block_size) ||
         (e4m3 && head_dim == 64))
@@ -226,6 +226,7 @@ yoco_status_t run_attn(const void* q, const void* k_cache, const void* v_cache,
     p.scale_log2 = scale * kLog2e;
     p.reverse = (flags & YOCO_ATTN_REVERSE) ? 1 : 0;
     p.overlap = (flags & YOCO_ATTN_OVERLAP) ? 1 : 0;
+    p.keep_tail = (flags & YOCO_ATTN_KEEP_TAIL) ? 1 : 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (pl.tc) {

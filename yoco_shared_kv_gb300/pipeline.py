@@ -156,6 +156,8 @@ class DeviceWorkload:
         selection, which writes cross_query_start_loc, so it does not."""
         d = ds.dev
         flags = N.YOCO_ATTN_REVERSE if (self.alternate and layer % 2 == 1) else 0
+        if self.alternate:  # the next layer starts where this one ends: keep that in L2
+            flags |= N.YOCO_ATTN_KEEP_TAIL
         if layer > 0:
             flags |= N.YOCO_ATTN_OVERLAP
         if self.e4m3:
@@ -193,7 +195,7 @@ class DeviceWorkload:
         N.yoco_cross_decode_step(d["q"][0], d["k_new"], d["v_new"], self.k_cache, self.v_cache,
                                  self.page_scales, ds.out[0], d["block_table"], d["seq_lens"],
                                  d["qsl"], ds.max_seq_len, self.wl.scale, ds.workspace, self.err,
-                                 stream)
+                                 stream, flags=N.YOCO_ATTN_KEEP_TAIL if self.alternate else 0)
         for layer in range(1, self.wl.layers if layers is None else layers):
             self.attend(ds, layer, stream, cq=d["qsl"])
 
