@@ -307,9 +307,11 @@ def run_ours(args, rank, world, local):
     g_step, g_attn = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_step, stream=stream):
         step_fn(step_i)
+    # the fused step runs no row selection: its cross query_start_loc is query_start_loc
+    cq = ds.dev["qsl"] if args.fused else None
     with torch.cuda.graph(g_attn, stream=stream):
         for layer in range(L):
-            dw.attend(ds, layer)
+            dw.attend(ds, layer, cq=cq)
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             g_step.replay()
@@ -354,7 +356,7 @@ def run_ours(args, rank, world, local):
             flush.zero_()
         with torch.cuda.graph(g_cold, stream=stream):
             flush.zero_()
-            dw.attend(ds, 0)
+            dw.attend(ds, 0, cq=cq)
         times = []
         for g in (g_fl, g_cold):
             c0 = torch.cuda.Event(enable_timing=True)
