@@ -724,18 +724,27 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
                         for (int c = 0; c < 4; ++c) sc[mt][nt][c] += sc2[mt][nt][c];
             }
             // ---- online softmax ----
+            // The scores stay unscaled: max(scale * s) = scale * max(s) for the positive
+            // scale, and the weights are exp2(fma(s, scale, -m)). Only a segment's last
+            // page can be partial; its keys past the causal end become -inf there.
+            if (nvalid < BS) {  // warp-uniform
+#pragma unroll
+                for (int mt = 0; mt < S::MT; ++mt)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const int t0 = mt * 16 + gl, t1 = t0 + 8;
+                        float* c = sc[mt][nt];
+                        if (t0 >= nvalid) c[0] = c[1] = -INFINITY;
+                        if (t1 >= nvalid) c[2] = c[3] = -INFINITY;
+                    }
+            }
             float corr[NT][2];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
                 for (int mt = 0; mt < S::MT; ++mt) {
-                    const int t0 = mt * 16 + gl, t1 = t0 + 8;
-                    float* c = sc[mt][nt];
-                    c[0] = t0 < nvalid ? c[0] * sl2p : -INFINITY;
-                    c[1] = t0 < nvalid ? c[1] * sl2p : -INFINITY;
-                    c[2] = t1 < nvalid ? c[2] * sl2p : -INFINITY;
-                    c[3] = t1 < nvalid ? c[3] * sl2p : -INFINITY;
+                    const float* c = sc[mt][nt];
                     mx0 = fmaxf(mx0, fmaxf(c[0], c[2]));
                     mx1 = fmaxf(mx1, fmaxf(c[1], c[3]));
                 }
@@ -744,7 +753,8 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
                     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
                     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
                 }
-                const float mn0 = fmaxf(m_run[nt][0], mx0), mn1 = fmaxf(m_run[nt][1], mx1);
+                const float mn0 = fmaxf(m_run[nt][0], mx0 * sl2p);
+                const float mn1 = fmaxf(m_run[nt][1], mx1 * sl2p);
                 corr[nt][0] = exp2_approx(m_run[nt][0] - mn0);
                 corr[nt][1] = exp2_approx(m_run[nt][1] - mn1);
                 m_run[nt][0] = mn0;
@@ -773,10 +783,10 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
                         const float* c = sc[kt][nt];
-                        const float p0 = exp2_approx(c[0] - m_run[nt][0]);
-                        const float p1 = exp2_approx(c[1] - m_run[nt][1]);
-                        const float p2 = exp2_approx(c[2] - m_run[nt][0]);
-                        const float p3 = exp2_approx(c[3] - m_run[nt][1]);
+                        const float p0 = exp2_approx(fmaf(c[0], sl2p, -m_run[nt][0]));
+                        const float p1 = exp2_approx(fmaf(c[1], sl2p, -m_run[nt][1]));
+                        const float p2 = exp2_approx(fmaf(c[2], sl2p, -m_run[nt][0]));
+                        const float p3 = exp2_approx(fmaf(c[3], sl2p, -m_run[nt][1]));
                         l_part[nt][0] += p0 + p2;
                         l_part[nt][1] += p1 + p3;
                         pb[kt][nt][0] = movmatrix_trans(pack_f16x2(p0 * vr, p1 * vr));
@@ -824,10 +834,10 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     const float* c = sc[kt][nt];
-                    const uint32_t lo = pack_bf16x2(exp2_approx(c[0] - m_run[nt][0]),
-                                                    exp2_approx(c[1] - m_run[nt][1]));
-                    const uint32_t hi = pack_bf16x2(exp2_approx(c[2] - m_run[nt][0]),
-                                                    exp2_approx(c[3] - m_run[nt][1]));
+                    const uint32_t lo = pack_bf16x2(exp2_approx(fmaf(c[0], sl2p, -m_run[nt][0])),
+                                                    exp2_approx(fmaf(c[1], sl2p, -m_run[nt][1])));
+                    const uint32_t hi = pack_bf16x2(exp2_approx(fmaf(c[2], sl2p, -m_run[nt][0])),
+                                                    exp2_approx(fmaf(c[3], sl2p, -m_run[nt][1])));
                     // row sums use exactly the rounded weights fed to the mma
                     l_part[nt][0] += bf16lo_to_f32(lo) + bf16lo_to_f32(hi);
                     l_part[nt][1] += bf16hi_to_f32(lo) + bf16hi_to_f32(hi);
