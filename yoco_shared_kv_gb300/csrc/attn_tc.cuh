@@ -234,7 +234,9 @@ __device__ __forceinline__ int32_t owner(int64_t x, int64_t P, int32_t workers) 
 constexpr int kMaxMergePieces = 1024;
 
 struct PieceHdr {
-    int64_t s0, s1;  // segment [first page, end) in the flattened order
+    int64_t s0, s1;    // segment [first page, end) in the flattened order
+    const float* o;    // [G][D] partial output: in the warp's ring or in the workspace
+    const float2* ml;  // [G] (m, l)
     int32_t n, g;
     int32_t valid;
 };
@@ -572,7 +574,6 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
     };
     const float sl2 = p.scale_log2;
     bool aborted = false;
-    int reload_slot = -1;  // slot of this warp's piece flushed mid-stream (to global memory)
     int consumed = 0;
     // one piece: [G][D] o, then [G] (m, l); 16-byte stride keeps float4 access aligned
     const int piece_bytes = (p.G * (D * 4 + 8) + 15) & ~15;
@@ -891,8 +892,8 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
                 const int slot = s0 < my_lo ? 0 : 1;
                 // A piece flushed at the end of the slice goes to this warp's
                 // ring, idle from here on; the one flushed mid-stream (the
-                // first segment walked) goes to global memory and is brought
-                // back into the ring after streaming.
+                // first segment walked) goes to the workspace, where the
+                // combine reads it.
                 const bool at_end = (i == n_my - 1);
                 float* dst_o;
                 float2* dst_ml;
@@ -903,7 +904,6 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
                     const int64_t piece = (static_cast<int64_t>(wid) * 2 + slot) * p.G;
                     dst_o = ws.w_o + piece * D;
                     dst_ml = ws.w_ml + piece;
-                    reload_slot = slot;
                 }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
@@ -925,6 +925,8 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
                     hdr[warp][slot].s1 = s1;
                     hdr[warp][slot].n = cc.n;
                     hdr[warp][slot].g = cc.g;
+                    hdr[warp][slot].o = dst_o;
+                    hdr[warp][slot].ml = dst_ml;
                     hdr[warp][slot].valid = 1;
                 }
             }
@@ -943,108 +945,81 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
             atomicExch(&abort_flag, 1);
         }
     }
-    if (reload_slot >= 0 && !aborted) {
-        // bring the mid-stream piece back next to the slice-end one
-        const int64_t piece = (static_cast<int64_t>(wid) * 2 + reload_slot) * p.G;
-        const float4* src = reinterpret_cast<const float4*>(ws.w_o + piece * D);
-        float4* dst = reinterpret_cast<float4*>(wbuf + reload_slot * piece_bytes);
-        const int nv = p.G * D / 4;
-        for (int v0 = lane; v0 < nv; v0 += 32 * 8) {  // 8 loads in flight per lane
-            float4 r[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                if (v0 + u * 32 < nv) r[u] = src[v0 + u * 32];
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                if (v0 + u * 32 < nv) dst[v0 + u * 32] = r[u];
-        }
-        float2* dml = reinterpret_cast<float2*>(
-            reinterpret_cast<float*>(wbuf + reload_slot * piece_bytes) + p.G * D);
-        for (int h = lane; h < p.G; h += 32) dml[h] = ws.w_ml[piece + h];
-    }
-    __syncthreads();  // pieces are in the warps' rings, headers in shared memory
+    __syncthreads();  // pieces and headers are visible to the whole CTA
     if (abort_flag) return;
 
     // ---- combine the pieces of each segment this CTA holds, in warp order ----
-    // Groups are consecutive valid pieces of one segment (at most 2 * NW). This
-    // code runs once per launch, right after streaming, with a cold instruction
-    // cache and L2 still busy with the other SMs' streams: it is kept short
-    // (plain loops) because each instruction fetch miss costs about a
-    // microsecond there, far more than the few shared-memory reads it does.
+    // A group is the run of valid pieces (warp, then slot order) of one
+    // segment. Threads are laid out head-major: each takes one head and every
+    // tph-th four-element vector of it, walks the groups itself and derives
+    // its head's scale factors once per pass over the pieces. So the combine
+    // has no barrier and no serial step: it runs once per launch, right after
+    // streaming, with a cold instruction cache and L2 still busy with the
+    // other SMs' streams, where each barrier or dependent step costs far more
+    // than the arithmetic.
     constexpr int MAXE = 2 * NW;
-    __shared__ float fac[MAXE][16];  // per piece and head: 2^(m - M) (/ L for an output)
-    __shared__ float2 seg_ml[16];    // per head: (M, L) of the combined piece
-    __shared__ int ent[MAXE];        // the group's valid pieces, in order
+    constexpr int D4 = D / 4;  // four-element vectors per head
     __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out);
-    auto piece_base = [&](int e) {   // e = warp * 2 + slot
-        return smem + (e >> 1) * STAGES * S::STAGE_BYTES + (e & 1) * piece_bytes;
-    };
+    const int tph = static_cast<int>(blockDim.x) / p.G;     // threads per head (G <= 16)
+    const int ch = static_cast<int>(threadIdx.x) / tph;     // this thread's head (G or more: idle)
+    const int cr = static_cast<int>(threadIdx.x) - ch * tph;
     int e0 = 0;
-    while (e0 < MAXE) {
-        if (!hdr[e0 >> 1][e0 & 1].valid) {
-            ++e0;
-            continue;
+    for (;;) {
+        while (e0 < MAXE && !hdr[e0 >> 1][e0 & 1].valid) ++e0;
+        if (e0 >= MAXE || ch >= p.G) break;
+        const int64_t s0 = hdr[e0 >> 1][e0 & 1].s0, s1 = hdr[e0 >> 1][e0 & 1].s1;
+        const int32_t gn = hdr[e0 >> 1][e0 & 1].n, gg = hdr[e0 >> 1][e0 & 1].g;
+        int e1 = e0 + 1;  // one past the group (entries in between may be invalid)
+        while (e1 < MAXE && (!hdr[e1 >> 1][e1 & 1].valid || hdr[e1 >> 1][e1 & 1].s0 == s0)) ++e1;
+        const bool whole = s0 >= cta_lo && s1 <= cta_hi;
+        const int h = ch;
+        float M = -INFINITY;
+#pragma unroll 4
+        for (int e = e0; e < e1; ++e) {
+            const PieceHdr& X = hdr[e >> 1][e & 1];
+            if (X.valid) M = fmaxf(M, X.ml[h].x);
         }
-        const PieceHdr H = hdr[e0 >> 1][e0 & 1];
-        int ne = 0, e1 = e0;
-        for (; e1 < MAXE; ++e1) {
-            const PieceHdr& X = hdr[e1 >> 1][e1 & 1];
-            if (!X.valid) continue;
-            if (X.s0 != H.s0) break;
-            if (threadIdx.x == 0) ent[ne] = e1;
-            ++ne;
-        }
-        const bool whole = H.s0 >= cta_lo && H.s1 <= cta_hi;
-        __syncthreads();  // ent[] is visible
-        if (threadIdx.x < p.G) {  // one thread per head builds the scale table
-            const int h = threadIdx.x;
-            float M = -INFINITY;
-#pragma unroll 1
-            for (int k = 0; k < ne; ++k)
-                M = fmaxf(M, reinterpret_cast<const float2*>(piece_base(ent[k]) + p.G * D * 4)[h].x);
+        const int64_t cp = (static_cast<int64_t>(blockIdx.x) * 2 + (s0 < cta_lo ? 0 : 1)) * p.G + h;
+        __nv_bfloat16* dsth = outp + (static_cast<int64_t>(gn) * p.H_q + gg * p.G + h) * D;
+        for (int c0 = cr; c0 < D4; c0 += 4 * tph) {  // up to four vectors per pass
+            float4 O[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) O[u] = make_float4(0.f, 0.f, 0.f, 0.f);
             float L = 0.f;
-#pragma unroll 1
-            for (int k = 0; k < ne; ++k) {
-                const float2 ml =
-                    reinterpret_cast<const float2*>(piece_base(ent[k]) + p.G * D * 4)[h];
+#pragma unroll 2
+            for (int e = e0; e < e1; ++e) {
+                const PieceHdr& X = hdr[e >> 1][e & 1];
+                if (!X.valid) continue;
+                const float2 ml = X.ml[h];
                 const float f = ml.x != -INFINITY ? exp2_approx(ml.x - M) : 0.f;
                 L += ml.y * f;
-                fac[k][h] = f;
+                const float4* xo = reinterpret_cast<const float4*>(X.o) + h * D4;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if (c0 + u * tph < D4) {
+                        const float4 x = xo[c0 + u * tph];
+                        O[u].x += x.x * f;
+                        O[u].y += x.y * f;
+                        O[u].z += x.z * f;
+                        O[u].w += x.w * f;
+                    }
+                }
             }
-            if (whole) {
-                const float inv = 1.f / L;
-#pragma unroll 1
-                for (int k = 0; k < ne; ++k) fac[k][h] *= inv;
+            const float inv = 1.f / L;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int j = c0 + u * tph;
+                if (j >= D4) continue;
+                if (whole) {
+                    __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(dsth + j * 4);
+                    dst[0] = __floats2bfloat162_rn(O[u].x * inv, O[u].y * inv);
+                    dst[1] = __floats2bfloat162_rn(O[u].z * inv, O[u].w * inv);
+                } else {
+                    reinterpret_cast<float4*>(ws.c_o + cp * D)[j] = O[u];
+                }
             }
-            seg_ml[h] = make_float2(M, L);
+            if (!whole && c0 == 0) ws.c_ml[cp] = make_float2(M, L);
         }
-        __syncthreads();
-        const int cslot = H.s0 < cta_lo ? 0 : 1;
-        const int64_t head0 = static_cast<int64_t>(H.n) * p.H_q + H.g * p.G;
-        const int nvec = p.G * D / 4;  // four consecutive elements (one head) per step
-        for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
-            const int h = (v * 4) / D;
-            float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 2
-            for (int k = 0; k < ne; ++k) {
-                const float4 x = reinterpret_cast<const float4*>(piece_base(ent[k]))[v];
-                const float fk = fac[k][h];
-                O.x += x.x * fk;
-                O.y += x.y * fk;
-                O.z += x.z * fk;
-                O.w += x.w * fk;
-            }
-            if (whole) {
-                __nv_bfloat16* dst = outp + head0 * D + v * 4;
-                reinterpret_cast<__nv_bfloat162*>(dst)[0] = __floats2bfloat162_rn(O.x, O.y);
-                reinterpret_cast<__nv_bfloat162*>(dst)[1] = __floats2bfloat162_rn(O.z, O.w);
-            } else {
-                const int64_t cp = (static_cast<int64_t>(blockIdx.x) * 2 + cslot) * p.G + h;
-                reinterpret_cast<float4*>(ws.c_o + cp * D)[(v * 4 - h * D) / 4] = O;
-                if (v * 4 - h * D == 0) ws.c_ml[cp] = seg_ml[h];
-            }
-        }
-        __syncthreads();  // the scale table is rewritten for the next group
         e0 = e1;
     }
     // the merge kernel may be scheduled now (it waits for this grid to finish);
