@@ -61,7 +61,8 @@ def test_e4m3_step_matches_oracle(P, idx):
 
 @pytest.mark.parametrize("H_q,H_kv,D,bs", [(8, 2, 128, 16), (16, 1, 256, 32), (4, 4, 128, 32),
                                            (32, 2, 256, 16), (6, 3, 256, 16), (16, 1, 128, 16),
-                                           (8, 2, 256, 32), (4, 1, 128, 32)])
+                                           (8, 2, 256, 32), (4, 1, 128, 32), (10, 2, 128, 32),
+                                           (12, 1, 256, 16)])
 def test_e4m3_shapes(P, H_q, H_kv, D, bs):
     wl = pure_decode(6000 + H_q * 7 + D, num_reqs=5, ctx_lo=1, ctx_hi=900, H_q=H_q, H_kv=H_kv,
                      D=D, bs=bs, layers=2)

@@ -181,7 +181,8 @@ def test_attention_single_key_and_block_edges(P):
 
 @pytest.mark.parametrize("H_q,H_kv,D,bs", [(4, 4, 64, 16), (6, 2, 128, 32), (12, 1, 64, 32),
                                            (16, 2, 256, 16), (2, 1, 128, 16), (16, 16, 128, 32),
-                                           (16, 1, 256, 32), (32, 2, 256, 16), (8, 1, 64, 16)])
+                                           (16, 1, 256, 32), (32, 2, 256, 16), (8, 1, 64, 16),
+                                           (10, 2, 128, 16), (7, 1, 256, 32)])
 def test_attention_shapes(P, H_q, H_kv, D, bs):
     wl = pure_decode(4000 + H_q * 7 + D, num_reqs=5, ctx_lo=1, ctx_hi=900, H_q=H_q, H_kv=H_kv,
                      D=D, bs=bs, layers=2)
