@@ -1045,8 +1045,6 @@ __global__ void __launch_bounds__(kMergeThreads) attn_tc_merge(const AttnParams 
     __shared__ float red[kMergeThreads];
     __shared__ float headM[2][16], headInvL[2][16];
     const int32_t c = blockIdx.x;
-    const int64_t cap64 = static_cast<int64_t>(p.max_blocks) * p.block_size;
-    const int32_t cap = cap64 > 0x7fffffff ? 0x7fffffff : static_cast<int32_t>(cap64);
     __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out);
     // launched as a programmatic dependent of attn_tc_persistent: wait for it,
     // and let the next kernel (the next layer's split) start its prologue
