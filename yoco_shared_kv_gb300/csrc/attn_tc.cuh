@@ -950,75 +950,117 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
 
     // ---- combine the pieces of each segment this CTA holds, in warp order ----
     // A group is the run of valid pieces (warp, then slot order) of one
-    // segment. Threads are laid out head-major: each takes one head and every
-    // tph-th four-element vector of it, walks the groups itself and derives
-    // its head's scale factors once per pass over the pieces. So the combine
-    // has no barrier and no serial step: it runs once per launch, right after
-    // streaming, with a cold instruction cache and L2 still busy with the
-    // other SMs' streams, where each barrier or dependent step costs far more
-    // than the arithmetic.
+    // segment. Every thread walks the groups itself and derives the scale
+    // factors it needs, so the combine has no barrier and no serial step: it
+    // runs once per launch, right after streaming, with a cold instruction
+    // cache and L2 still busy with the other SMs' streams, where each barrier
+    // or dependent step costs far more than the arithmetic. Groups of up to 8
+    // heads (one tile) take one four-element vector per thread and step; wider
+    // groups lay the threads out head-major, each taking one head and every
+    // tph-th vector of it, so the factors are derived once per head, not once
+    // per vector.
     constexpr int MAXE = 2 * NW;
     constexpr int D4 = D / 4;  // four-element vectors per head
     __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out);
     const int tph = static_cast<int>(blockDim.x) / p.G;     // threads per head (G <= 16)
     const int ch = static_cast<int>(threadIdx.x) / tph;     // this thread's head (G or more: idle)
-    const int cr = static_cast<int>(threadIdx.x) - ch * tph;
+    const int nvec = p.G * D4;  // four-element vectors of a segment's output
     int e0 = 0;
     for (;;) {
         while (e0 < MAXE && !hdr[e0 >> 1][e0 & 1].valid) ++e0;
-        if (e0 >= MAXE || ch >= p.G) break;
+        if (e0 >= MAXE || (NT != 1 && ch >= p.G)) break;
         const int64_t s0 = hdr[e0 >> 1][e0 & 1].s0, s1 = hdr[e0 >> 1][e0 & 1].s1;
         const int32_t gn = hdr[e0 >> 1][e0 & 1].n, gg = hdr[e0 >> 1][e0 & 1].g;
         int e1 = e0 + 1;  // one past the group (entries in between may be invalid)
         while (e1 < MAXE && (!hdr[e1 >> 1][e1 & 1].valid || hdr[e1 >> 1][e1 & 1].s0 == s0)) ++e1;
         const bool whole = s0 >= cta_lo && s1 <= cta_hi;
-        const int h = ch;
-        float M = -INFINITY;
+        if constexpr (NT == 1) {
+            const int cslot = s0 < cta_lo ? 0 : 1;
+            const int64_t head0 = static_cast<int64_t>(gn) * p.H_q + gg * p.G;
+            for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+                const int h = (v * 4) / D;
+                float M = -INFINITY;
 #pragma unroll 4
-        for (int e = e0; e < e1; ++e) {
-            const PieceHdr& X = hdr[e >> 1][e & 1];
-            if (X.valid) M = fmaxf(M, X.ml[h].x);
-        }
-        const int64_t cp = (static_cast<int64_t>(blockIdx.x) * 2 + (s0 < cta_lo ? 0 : 1)) * p.G + h;
-        __nv_bfloat16* dsth = outp + (static_cast<int64_t>(gn) * p.H_q + gg * p.G + h) * D;
-        for (int c0 = cr; c0 < D4; c0 += 4 * tph) {  // up to four vectors per pass
-            float4 O[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) O[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            float L = 0.f;
+                for (int e = e0; e < e1; ++e) {
+                    const PieceHdr& X = hdr[e >> 1][e & 1];
+                    if (X.valid) M = fmaxf(M, X.ml[h].x);
+                }
+                float L = 0.f;
+                float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 2
+                for (int e = e0; e < e1; ++e) {
+                    const PieceHdr& X = hdr[e >> 1][e & 1];
+                    if (!X.valid) continue;
+                    const float2 ml = X.ml[h];
+                    const float4 x = reinterpret_cast<const float4*>(X.o)[v];
+                    const float f = ml.x != -INFINITY ? exp2_approx(ml.x - M) : 0.f;
+                    L += ml.y * f;
+                    O.x += x.x * f;
+                    O.y += x.y * f;
+                    O.z += x.z * f;
+                    O.w += x.w * f;
+                }
+                if (whole) {
+                    const float inv = 1.f / L;
+                    __nv_bfloat16* dst = outp + head0 * D + v * 4;
+                    reinterpret_cast<__nv_bfloat162*>(dst)[0] = __floats2bfloat162_rn(O.x * inv, O.y * inv);
+                    reinterpret_cast<__nv_bfloat162*>(dst)[1] = __floats2bfloat162_rn(O.z * inv, O.w * inv);
+                } else {
+                    const int64_t cp = (static_cast<int64_t>(blockIdx.x) * 2 + cslot) * p.G + h;
+                    reinterpret_cast<float4*>(ws.c_o + cp * D)[(v * 4 - h * D) / 4] = O;
+                    if (v * 4 - h * D == 0) ws.c_ml[cp] = make_float2(M, L);
+                }
+            }
+        } else {
+            const int cr = static_cast<int>(threadIdx.x) - ch * tph;
+            const int h = ch;
+            float M = -INFINITY;
+#pragma unroll 4
             for (int e = e0; e < e1; ++e) {
                 const PieceHdr& X = hdr[e >> 1][e & 1];
-                if (!X.valid) continue;
-                const float2 ml = X.ml[h];
-                const float f = ml.x != -INFINITY ? exp2_approx(ml.x - M) : 0.f;
-                L += ml.y * f;
-                const float4* xo = reinterpret_cast<const float4*>(X.o) + h * D4;
+                if (X.valid) M = fmaxf(M, X.ml[h].x);
+            }
+            const int64_t cp = (static_cast<int64_t>(blockIdx.x) * 2 + (s0 < cta_lo ? 0 : 1)) * p.G + h;
+            __nv_bfloat16* dsth = outp + (static_cast<int64_t>(gn) * p.H_q + gg * p.G + h) * D;
+            for (int c0 = cr; c0 < D4; c0 += 4 * tph) {  // up to four vectors per pass
+                float4 O[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    if (c0 + u * tph < D4) {
-                        const float4 x = xo[c0 + u * tph];
-                        O[u].x += x.x * f;
-                        O[u].y += x.y * f;
-                        O[u].z += x.z * f;
-                        O[u].w += x.w * f;
+                for (int u = 0; u < 4; ++u) O[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                float L = 0.f;
+#pragma unroll 2
+                for (int e = e0; e < e1; ++e) {
+                    const PieceHdr& X = hdr[e >> 1][e & 1];
+                    if (!X.valid) continue;
+                    const float2 ml = X.ml[h];
+                    const float f = ml.x != -INFINITY ? exp2_approx(ml.x - M) : 0.f;
+                    L += ml.y * f;
+                    const float4* xo = reinterpret_cast<const float4*>(X.o) + h * D4;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        if (c0 + u * tph < D4) {
+                            const float4 x = xo[c0 + u * tph];
+                            O[u].x += x.x * f;
+                            O[u].y += x.y * f;
+                            O[u].z += x.z * f;
+                            O[u].w += x.w * f;
+                        }
                     }
                 }
-            }
-            const float inv = 1.f / L;
+                const float inv = 1.f / L;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int j = c0 + u * tph;
-                if (j >= D4) continue;
-                if (whole) {
-                    __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(dsth + j * 4);
-                    dst[0] = __floats2bfloat162_rn(O[u].x * inv, O[u].y * inv);
-                    dst[1] = __floats2bfloat162_rn(O[u].z * inv, O[u].w * inv);
-                } else {
-                    reinterpret_cast<float4*>(ws.c_o + cp * D)[j] = O[u];
+                for (int u = 0; u < 4; ++u) {
+                    const int j = c0 + u * tph;
+                    if (j >= D4) continue;
+                    if (whole) {
+                        __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(dsth + j * 4);
+                        dst[0] = __floats2bfloat162_rn(O[u].x * inv, O[u].y * inv);
+                        dst[1] = __floats2bfloat162_rn(O[u].z * inv, O[u].w * inv);
+                    } else {
+                        reinterpret_cast<float4*>(ws.c_o + cp * D)[j] = O[u];
+                    }
                 }
+                if (!whole && c0 == 0) ws.c_ml[cp] = make_float2(M, L);
             }
-            if (!whole && c0 == 0) ws.c_ml[cp] = make_float2(M, L);
         }
         e0 = e1;
     }
