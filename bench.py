@@ -509,10 +509,9 @@ def oracle_step(wl, step, Ks, Vs, kp, vp, nthreads, layers=None, rows=None):
         oracle.cross_attn(q, Ks, Vs, step.seq_lens, cqsl, wl.scale, rows=rows, nthreads=nthreads)
 
 
-def _oracle_setup(wl, step, rows):
+def _oracle_setup(wl, step):
+    """Each scheduled request's contiguous K/V, widened for the oracle."""
     import oracle
-    reqs = sorted(set(step.req_ids[i] for i in range(step.num_reqs)))
-    del reqs
     Ks, Vs = [], []
     for r in step.req_ids:
         K, V = wl.request_kv(r)
@@ -526,7 +525,7 @@ def cpu_baseline(wl, step_i: int, budget_s: float = 20.0) -> dict:
     step = wl.steps[step_i]
     acc = accounting(wl, step)
     nthreads = host_cores()
-    Ks, Vs = _oracle_setup(wl, step, None)
+    Ks, Vs = _oracle_setup(wl, step)
     kp, vp = wl.empty_pool(), wl.empty_pool()
     kv_lens = cross_rows_kv_lens(step)
     # sample: all rows, layers taken one at a time until the budget is spent
@@ -553,7 +552,7 @@ def run_reference(args, rank, world):
     step = wl.steps[step_i]
     acc = accounting(wl, step)
     nthreads = host_cores()
-    Ks, Vs = _oracle_setup(wl, step, None)
+    Ks, Vs = _oracle_setup(wl, step)
     kp, vp = wl.empty_pool(), wl.empty_pool()
     # a reference step is the step's append + select + a bounded number of
     # layers over all rows, sized so the whole run stays within minutes
