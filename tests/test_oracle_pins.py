@@ -330,3 +330,21 @@ def test_widen_bf16_exact():
     assert got[2] == 3.140625
     assert got[3] == 2.0 ** -133  # smallest bf16 subnormal
     assert got[4] == (2 - 2 ** -7) * 2.0 ** 127  # largest finite bf16
+
+
+def test_attn_row_wrapper_closed_forms():
+    """The single-row entry point, directly: only the first kv_len keys count
+    (two-key logistic weight), and one key returns V exactly per kv head."""
+    q = np.array([[1.0, 0.0]])
+    K = np.array([[[1.0, 0.0]], [[0.0, 1.0]], [[50.0, 0.0]]])  # the third key lies past kv_len
+    V = np.array([[[1.0, 2.0]], [[3.0, 4.0]], [[-9.0, -9.0]]])
+    sig = 0.66976155  # logistic(1/sqrt(2)), worked by hand
+    out = oracle.attn_row(q, K, V, 2, 1 / math.sqrt(2))
+    np.testing.assert_allclose(out[0], [sig * 1 + (1 - sig) * 3, sig * 2 + (1 - sig) * 4], atol=1e-8)
+    rng = np.random.default_rng(4)
+    K1 = rng.standard_normal((3, 2, 8))
+    V1 = rng.standard_normal((3, 2, 8))
+    q1 = rng.standard_normal((6, 8)) * 10
+    out1 = oracle.attn_row(q1, K1, V1, 1, 0.3)
+    for h in range(6):
+        assert np.array_equal(out1[h], V1[0, h // 3])
