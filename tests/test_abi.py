@@ -164,3 +164,30 @@ def test_fused_step_host_validation(lib_path):
     assert L.yoco_cross_attn_paged_noalloc(fake, fake, fake, fake, fake, 4, fake, fake, 1, 1, 64,
                                            8, 2, 256, 16, 100, 0.0625, N.YOCO_E4M3, None,
                                            None) == N.YOCO_ERR_UNSUPPORTED
+
+
+def test_append_host_validation(lib_path):
+    """yoco_kv_append rejects bad arguments before any CUDA call (the pointers
+    below are never dereferenced), and an empty batch is a no-op."""
+    from yoco_shared_kv_gb300 import _native as N
+    L = N.lib
+    fake = 1 << 20
+
+    def app(**kw):
+        a = dict(kn=fake, kc=fake, maxb=4, R=1, T=1, nb=100, bs=16, hkv=2, d=128, dt=N.YOCO_BF16)
+        a.update(kw)
+        return L.yoco_kv_append(a["kn"], fake, a["kc"], fake, fake, a["maxb"], fake, fake, a["R"],
+                                a["T"], a["nb"], a["bs"], a["hkv"], a["d"], a["dt"], None, None)
+    assert app(dt=N.YOCO_E4M3) == N.YOCO_ERR_UNSUPPORTED  # the 8-bit cache has its own entry
+    assert app(dt=7) == N.YOCO_ERR_UNSUPPORTED
+    assert app(d=96) == N.YOCO_ERR_UNSUPPORTED
+    assert app(bs=24) == N.YOCO_ERR_UNSUPPORTED
+    assert app(R=-1) == N.YOCO_ERR_INVALID_ARG
+    assert app(T=-1) == N.YOCO_ERR_INVALID_ARG
+    assert app(nb=0) == N.YOCO_ERR_INVALID_ARG
+    assert app(hkv=0) == N.YOCO_ERR_INVALID_ARG
+    assert app(maxb=0) == N.YOCO_ERR_INVALID_ARG
+    assert app(kn=None) == N.YOCO_ERR_INVALID_ARG
+    assert app(kc=fake + 8) == N.YOCO_ERR_INVALID_ARG    # 16-byte vector stores need alignment
+    assert app(T=0, kn=None, kc=None) == N.YOCO_OK       # nothing to append: no launch
+    assert app(R=0, kn=None, kc=None) == N.YOCO_OK
