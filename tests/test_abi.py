@@ -191,3 +191,30 @@ def test_append_host_validation(lib_path):
     assert app(kc=fake + 8) == N.YOCO_ERR_INVALID_ARG    # 16-byte vector stores need alignment
     assert app(T=0, kn=None, kc=None) == N.YOCO_OK       # nothing to append: no launch
     assert app(R=0, kn=None, kc=None) == N.YOCO_OK
+
+
+def test_noalloc_and_l2_window_host_validation(lib_path):
+    """The allocation-free entry refuses the 8-bit dtype and bounds its fixed
+    array cannot hold, and the L2 window refuses a hit ratio above 1, all
+    before any CUDA call (the pointers are never dereferenced)."""
+    import torch
+    from yoco_shared_kv_gb300 import _native as N
+    L = N.lib
+    fake = 1 << 20
+    cap = N.yoco_cross_attn_noalloc_capacity()
+    assert cap > 0
+
+    def noalloc(dt, H_q=8, H_kv=2, D=256, bs=16, rows=4, ctx=4096):
+        return L.yoco_cross_attn_paged_noalloc(fake, fake, fake, fake, fake, 4, fake, fake, 1, rows,
+                                               ctx, H_q, H_kv, D, bs, 100, ctypes.c_float(0.0625),
+                                               dt, None, None)
+    assert noalloc(N.YOCO_E4M3) == N.YOCO_ERR_UNSUPPORTED
+    assert noalloc(9) == N.YOCO_ERR_UNSUPPORTED
+    # a 16-wide group at head_dim 256 needs more scratch than the array holds
+    assert N.yoco_cross_attn_workspace_size(4, 16, 1, 256, 16, 4096, torch.bfloat16) > cap
+    assert noalloc(N.YOCO_BF16, H_q=16, H_kv=1) == N.YOCO_ERR_WORKSPACE
+    L.yoco_set_l2_window.restype = ctypes.c_int
+    L.yoco_set_l2_window.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                     ctypes.c_float]
+    assert L.yoco_set_l2_window(None, fake, 1 << 20, 1.5) == N.YOCO_ERR_INVALID_ARG
+    assert L.yoco_set_l2_window(None, fake, 1 << 20, float("nan")) == N.YOCO_ERR_INVALID_ARG
