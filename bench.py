@@ -64,6 +64,8 @@ def parse_args(argv=None):
                     help="cache format: the workload's dtype, or e4m3 with per-page scales")
     ap.add_argument("--fused", action="store_true",
                     help="decode workloads: fuse the append into layer 0 (yoco_cross_decode_step)")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time only the configured workload (no per_config block)")
     return ap.parse_args(argv)
 
 
@@ -240,46 +242,97 @@ def aggregate_ranks(elapsed_ms: float, kv_bytes: float, rows: float, world: int,
 # --------------------------------------------------------------- our arm
 
 
-def run_ours(args, rank, world, local):
+def _graph_time_ms(g, stream, reps, warm=3):
+    """Average replay time of CUDA graph g on `stream` (CUDA events, after warm-up)."""
     import torch
-    from yoco_shared_kv_gb300 import build as B
-    if rank == 0 or not os.path.exists(B.LIB):
-        B.build()
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
+    c0 = torch.cuda.Event(enable_timing=True)
+    c1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for _ in range(warm):
+            g.replay()
+        c0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        c1.record(stream)
+    stream.synchronize()
+    return c0.elapsed_time(c1) / reps
+
+
+def cold_layer_ms(dw, ds, cq, stream, dev, reps):
+    """One layer (layer 0) from an L2 that holds none of the cache, two ways.
+
+    clean: the L2 is first filled by READING a buffer of 2 x L2 (a reduction),
+    so it holds only clean, unrelated lines; the layer's DRAM traffic is its own.
+    dirty: the L2 is first filled by WRITING 2 x L2 (a memset); the layer then
+    also pays for writing back the ~L2 of dirty lines it evicts.
+    Each is graph(flush, layer 0) minus graph(flush), CUDA events."""
+    import torch
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.zeros(2 * l2 // 4, dtype=torch.int32, device=dev)
+    sink = torch.zeros(1, dtype=torch.int64, device=dev)
+    out = {}
+    for kind in ("clean", "dirty"):
+        def fl():
+            if kind == "clean":
+                torch.sum(flush, out=sink)
+            else:
+                flush.zero_()
+        g_fl, g_cold = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_fl, stream=stream):
+            fl()
+        with torch.cuda.graph(g_cold, stream=stream):
+            fl()
+            dw.attend(ds, 0, cq=cq)
+        t_fl = _graph_time_ms(g_fl, stream, reps)
+        t_cold = _graph_time_ms(g_cold, stream, reps)
+        out[kind] = max(t_cold - t_fl, 1e-6)
+        del g_fl, g_cold
+    del flush
+    return out
+
+
+def measure(args, config, rank, world, local, *, kv="native", fused=False, steps=None,
+            warmup=None, e2e=True, cold=True, l2_window=False, alternate=True, reqs=None,
+            seed_offset=0):
+    """Time one workload through the whole path on this rank's GPU.
+
+    Returns the record of one bench line (without clocks or the CPU baseline):
+    the step's logical KV GB/s, query rows/s, the dominant kernel's launch
+    figures, one layer from a cold L2, and the end-to-end figure with host
+    copies."""
+    import torch
     from yoco_shared_kv_gb300 import _native as N
     from yoco_shared_kv_gb300 import pipeline as P
 
-    torch.cuda.set_device(local)
+    steps = args.steps if steps is None else steps
+    warmup = args.warmup if warmup is None else warmup
     dev = torch.device("cuda", local)
-    wl = make_workload(args.config, rank, args.reqs, args.seed_offset)
-    e4m3 = args.kv == "e4m3"
+    wl = make_workload(config, rank, reqs, seed_offset)
+    e4m3 = kv == "e4m3"
+    if e4m3 and wl.dtype != "bf16":
+        return None
     if e4m3:
         from workloads import page_scales
-        dw = P.DeviceWorkload(wl, dev, pin_host=not args.no_e2e, sentinel=False, kv="e4m3",
+        dw = P.DeviceWorkload(wl, dev, pin_host=e2e, sentinel=False, kv="e4m3",
                               page_scales=page_scales(wl))
     else:
-        dw = P.DeviceWorkload(wl, dev, pin_host=not args.no_e2e, sentinel=False)
-    if args.no_alternate:
+        dw = P.DeviceWorkload(wl, dev, pin_host=e2e, sentinel=False)
+    if not alternate:
         dw.alternate = False
     step_i = len(wl.steps) - 1
     ds = dw.steps[step_i]
     acc = accounting(wl, wl.steps[step_i], e4m3)
     workload_name = wl.name + ("_e4m3kv" if e4m3 else "")
-    if args.fused and not dw.decode_only(step_i):
+    if fused and not dw.decode_only(step_i):
         raise SystemExit("--fused needs a decode-only workload (one token and one row per request)")
 
-    def step_fn(i):
-        step_fn_on(dw.steps[i])
-
     def step_fn_on(d_s):
-        if args.fused:
+        if fused:
             dw.fused_step_on(d_s)
         else:
             dw.run_step_on(d_s)
     stream = torch.cuda.Stream(device=dev)
-    if args.l2_window:  # before capture: the kernel nodes take the stream's window
+    if l2_window:  # before capture: the kernel nodes take the stream's window
         N.yoco_set_l2_window(dw.k_cache, dw.k_cache.numel() * dw.k_cache.element_size(), -1.0,
                              stream=stream)
     with torch.cuda.stream(stream):
@@ -288,32 +341,30 @@ def run_ours(args, rank, world, local):
             dw.run_step(i, stream)
     stream.synchronize()
 
-    ws_bytes = ds.workspace.numel() if ds.workspace is not None else 0
     merges = 1 if N.yoco_cross_attn_workspace_size(max(ds.rows_upper, 1), wl.num_q_heads,
                                                    wl.num_kv_heads, wl.head_dim, wl.block_size,
                                                    ds.max_seq_len,
                                                    torch.float8_e4m3fn if e4m3
                                                    else P.torch_dtype(wl.dtype)) > 0 else 0
-    launches_per_step = (0 if args.fused else 2) + wl.layers * (1 + merges)
+    launches_per_step = (0 if fused else 2) + wl.layers * (1 + merges)
 
-    sampler = None if args.no_clocks else ClockSampler(local)
     L = wl.layers
     # The step runs as one CUDA graph (append -> select -> every layer), as an
     # engine replays its captured cross-decoder; a second graph holds only the
     # L attention calls, to time the dominant kernel on its own.
     with torch.cuda.stream(stream):
-        step_fn(step_i)  # eager once: one-time host set-up before capture
+        step_fn_on(ds)  # eager once: one-time host set-up before capture
     stream.synchronize()
     g_step, g_attn = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_step, stream=stream):
-        step_fn(step_i)
+        step_fn_on(ds)
     # the fused step runs no row selection: its cross query_start_loc is query_start_loc
-    cq = ds.dev["qsl"] if args.fused else None
+    cq = ds.dev["qsl"] if fused else None
     with torch.cuda.graph(g_attn, stream=stream):
         for layer in range(L):
             dw.attend(ds, layer, cq=cq)
     with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
+        for _ in range(warmup):
             g_step.replay()
     stream.synchronize()
     if world > 1:
@@ -322,60 +373,21 @@ def run_ours(args, rank, world, local):
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(dev)
-    if sampler:
-        sampler.mark_start()
     with torch.cuda.stream(stream):
         ev0.record(stream)
-        for _ in range(args.steps):
+        for _ in range(steps):
             g_step.replay()
         ev1.record(stream)
     stream.synchronize()
     torch.cuda.synchronize(dev)
-    if sampler:
-        sampler.mark_stop()
     elapsed_ms = ev0.elapsed_time(ev1)
     # dominant kernel: the attention calls alone, same inputs, CUDA events
-    a0 = torch.cuda.Event(enable_timing=True)
-    a1 = torch.cuda.Event(enable_timing=True)
-    reps = max(3, args.steps // 2)
-    with torch.cuda.stream(stream):
-        g_attn.replay()
-        a0.record(stream)
-        for _ in range(reps):
-            g_attn.replay()
-        a1.record(stream)
-    stream.synchronize()
-    attn_launch_ms = a0.elapsed_time(a1) / (reps * L)
-    # one layer from a cold L2: a graph of (flush, layer 0) minus a graph of the flush alone
-    cold_ms = None
-    if not args.no_cold:
-        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-        flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
-        g_fl, g_cold = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_fl, stream=stream):
-            flush.zero_()
-        with torch.cuda.graph(g_cold, stream=stream):
-            flush.zero_()
-            dw.attend(ds, 0, cq=cq)
-        times = []
-        for g in (g_fl, g_cold):
-            c0 = torch.cuda.Event(enable_timing=True)
-            c1 = torch.cuda.Event(enable_timing=True)
-            with torch.cuda.stream(stream):
-                for _ in range(3):
-                    g.replay()
-                c0.record(stream)
-                for _ in range(reps):
-                    g.replay()
-                c1.record(stream)
-            stream.synchronize()
-            times.append(c0.elapsed_time(c1) / reps)
-        cold_ms = max(times[1] - times[0], 1e-6)
-        del flush
+    reps = max(3, steps // 2)
+    attn_launch_ms = _graph_time_ms(g_attn, stream, reps, warm=1) / L
+    cold_ms = cold_layer_ms(dw, ds, cq, stream, dev, reps) if cold else None
 
     max_ms, total_kv_bytes, total_rows = aggregate_ranks(
-        elapsed_ms, acc["kv_bytes_step"] * args.steps, acc["rows"] * L * args.steps, world, dev)
-    clocks = sampler.stop() if sampler else None
+        elapsed_ms, acc["kv_bytes_step"] * steps, acc["rows"] * L * steps, world, dev)
     if dw.error_bits() != 0:
         raise RuntimeError(f"device error bits {dw.error_bits():#x}")
 
@@ -384,8 +396,8 @@ def run_ours(args, rank, world, local):
     # alternate, so the copies of one step overlap the computation of another
     # (copy-in stream, compute stream, read-back stream, ordered by events); the
     # timed region covers every copy.
-    e2e = None
-    if not args.no_e2e:
+    e2e_rec = None
+    if e2e:
         ds_b = dw.step_buffers(step_i)
         g_b = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
@@ -399,7 +411,7 @@ def run_ours(args, rank, world, local):
         ev_in = [torch.cuda.Event() for _ in bufs]
         ev_done = [torch.cuda.Event() for _ in bufs]
         ev_read = [torch.cuda.Event() for _ in bufs]
-        k_e2e = max(1, min(args.steps, 200))
+        k_e2e = max(1, min(steps, 200))
         warm = 4
         h2d = d2h = 0
         e0 = torch.cuda.Event(enable_timing=True)
@@ -438,53 +450,140 @@ def run_ours(args, rank, world, local):
             t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             e2e_ms = float(t[0])
-        e2e = {"value": round(total_kv_bytes / args.steps / (e2e_ms / 1e3) / 1e9, 3), "unit": "GB/s",
-               "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h),
-               "how": "two input/output buffer sets; copies overlap the other set's step"}
+        e2e_rec = {"value": round(total_kv_bytes / steps / (e2e_ms / 1e3) / 1e9, 3),
+                   "unit": "GB/s", "ms_per_step": round(e2e_ms, 4),
+                   "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                   "how": "two input/output buffer sets; copies overlap the other set's step"}
+        del g_b, ds_b
+    if l2_window:
+        N.yoco_set_l2_window(None, 0, stream=stream)
 
-    ms_per_step = max_ms / args.steps
+    ms_per_step = max_ms / steps
     value = total_kv_bytes / (max_ms / 1e3) / 1e9
     peaks = measured_peaks()
+    peak = peaks["hbm_gbs"]
     achieved = acc["attn_bytes_layer"] / (attn_launch_ms / 1e3) / 1e9
     traffic = profiled_traffic(workload_name)
+
+    def cold_rec(ms, how):
+        gbs = acc["attn_bytes_layer"] / (ms / 1e3) / 1e9
+        return {"launch_ms": round(ms, 5), "achieved_gbs": round(gbs, 2),
+                "frac": round(gbs / peak, 4), "how": how}
     res = {
         "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "steps": steps, "warmup": warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 cache, bf16 q/out, f16 mma" if e4m3 else wl.dtype,
         "data": "synthetic (seeded N(0,1) K/V and queries, random page permutation)",
-        "config": {
-            "workload": workload_name, "description": wl.description, "H_q": wl.num_q_heads,
-            "H_kv": wl.num_kv_heads, "head_dim": wl.head_dim, "block_size": wl.block_size,
-            "layers": wl.layers, "requests": wl.steps[step_i].num_reqs,
-            "step_tokens": wl.steps[step_i].num_tokens, "cross_rows": acc["rows"],
-            "kv_bytes_per_layer": acc["kv_bytes_layer"],
-            "l2": ("inputs larger than L2" if acc["kv_bytes_layer"] > 129e6
-                   else "inputs fit in L2 (layers re-read them: logical bytes)"),
-            "parallelism": f"replicas x{world}",
-            "step": ("append fused into layer 0 (yoco_cross_decode_step)" if args.fused
-                     else "append, select, every layer"),
-        },
-        "hbm_frac": round(value / peaks["hbm_gbs"], 4),
+        "config": workload_config(wl, wl.steps[step_i], acc, world, fused, workload_name),
+        "hbm_frac": round(value / peak, 4),
         "query_rows_per_s": round(total_rows / (max_ms / 1e3), 1),
         "roofline": {"kernel": DOMINANT_KERNEL + " (+ split merge)", "bound": "hbm",
-                     "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+                     "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     # DRAM-side fraction: the bytes DRAM actually moved per launch
+                     # inside the layer sequence (ncu), over the same launch time
+                     "dram_frac": (None if traffic is None else
+                                   round(traffic / (attn_launch_ms / 1e3) / 1e9 / peak, 4)),
                      "algorithmic_bytes_per_launch": acc["attn_bytes_layer"],
                      "launch_ms": round(attn_launch_ms, 5), "peak_source": peaks["source"]},
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clocks,
-        "per_layer_cold_l2": None if cold_ms is None else {
-            "launch_ms": round(cold_ms, 5),
-            "achieved_gbs": round(acc["attn_bytes_layer"] / (cold_ms / 1e3) / 1e9, 2),
-            "frac": round(acc["attn_bytes_layer"] / (cold_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
-            "how": "graph(flush 2 x L2 with a memset, layer 0) minus graph(flush), CUDA events"},
+        "gpu_launches": launches_per_step * steps,
+        "per_layer_cold_l2": None if cold_ms is None else cold_rec(
+            cold_ms["clean"], "graph(read 2 x L2 with a reduction, layer 0) minus graph(the "
+            "reduction), CUDA events: the L2 holds only clean lines of another buffer"),
+        "per_layer_cold_l2_dirty": None if cold_ms is None else cold_rec(
+            cold_ms["dirty"], "graph(memset 2 x L2, layer 0) minus graph(memset): the layer "
+            "also writes back the dirty lines it evicts"),
     }
-    if e2e is not None:
-        res["e2e"] = e2e
+    if e2e_rec is not None:
+        res["e2e"] = e2e_rec
+    res["_wl"] = wl
+    res["_step_i"] = step_i
+    del g_step, g_attn, dw, ds
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    return res
+
+
+def _compact(r: dict) -> dict:
+    """The per-workload figures of a measure() record, for the per_config block."""
+    if r is None:
+        return None
+    out = {"workload": r["config"]["workload"], "value": r["value"], "unit": r["unit"],
+           "ms_per_step": r["ms_per_step"], "hbm_frac": r["hbm_frac"],
+           "query_rows_per_s": r["query_rows_per_s"], "steps": r["steps"],
+           "roofline": {k: r["roofline"][k] for k in ("achieved", "frac", "dram_frac",
+                                                      "traffic", "launch_ms")}}
+    for k in ("per_layer_cold_l2", "per_layer_cold_l2_dirty"):
+        if r.get(k):
+            out[k] = {"frac": r[k]["frac"], "achieved_gbs": r[k]["achieved_gbs"],
+                      "launch_ms": r[k]["launch_ms"]}
+    if r.get("e2e"):
+        out["e2e"] = {"value": r["e2e"]["value"], "ms_per_step": r["e2e"]["ms_per_step"]}
+    if r.get("cpu_baseline"):
+        out["cpu_baseline"] = r["cpu_baseline"]
+    return out
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    from yoco_shared_kv_gb300 import build as B
+    if rank == 0 or not os.path.exists(B.LIB):
+        B.build()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.set_device(local)
+
+    sampler = None if args.no_clocks else ClockSampler(local)
+    if sampler:
+        sampler.mark_start()
+    res = measure(args, args.config, rank, world, local, kv=args.kv, fused=args.fused,
+                  e2e=not args.no_e2e, cold=not args.no_cold, l2_window=args.l2_window,
+                  alternate=not args.no_alternate, reqs=args.reqs, seed_offset=args.seed_offset)
+    if sampler:
+        sampler.mark_stop()
+    wl, step_i = res.pop("_wl"), res.pop("_step_i")
+    e4m3 = args.kv == "e4m3"
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not e4m3:
         res["cpu_baseline"] = cpu_baseline(wl, step_i)
+    del wl
+
+    # Every workload of the problem statement, the 8-bit cache and the fused
+    # decode step, each timed the same way (fewer steps), so that one default
+    # run observes them all; the headline above is the configured workload.
+    if not args.no_per_config and args.reqs is None and world == 1:
+        sub_steps = max(3, min(args.steps, 30))
+        sub_warm = max(3, min(args.warmup, 5))
+        per = {}
+        for c in range(5):
+            if c == args.config and not args.fused and args.kv == "native":
+                r = dict(res)
+            else:
+                r = measure(args, c, rank, world, local, steps=sub_steps, warmup=sub_warm,
+                            e2e=not args.no_e2e, cold=not args.no_cold)
+                wl_c, si = r.pop("_wl"), r.pop("_step_i")
+                if rank == 0 and not args.no_cpu_baseline:
+                    r["cpu_baseline"] = cpu_baseline(wl_c, si, budget_s=3.0, one_thread_s=1.5)
+                del wl_c
+            per[str(c)] = _compact(r)
+        res["per_config"] = per
+        e8 = {}
+        for c in range(1, 5):
+            r = measure(args, c, rank, world, local, kv="e4m3", steps=sub_steps,
+                        warmup=sub_warm, e2e=False, cold=not args.no_cold)
+            r.pop("_wl"), r.pop("_step_i")
+            e8[str(c)] = _compact(r)
+        res["per_config_e4m3"] = e8
+        fu = {}
+        for kv in ("native", "e4m3"):
+            r = measure(args, 1, rank, world, local, kv=kv, fused=True, steps=sub_steps,
+                        warmup=sub_warm, e2e=False, cold=False)
+            r.pop("_wl"), r.pop("_step_i")
+            fu[kv] = {"workload": r["config"]["workload"], "ms_per_step": r["ms_per_step"],
+                      "value": r["value"], "query_rows_per_s": r["query_rows_per_s"]}
+        res["fused_decode_step"] = fu
+    res["clocks"] = sampler.stop() if sampler else None
     return res
 
 
@@ -520,15 +619,19 @@ def _oracle_setup(wl, step):
     return Ks, Vs
 
 
-def cpu_baseline(wl, step_i: int, budget_s: float = 20.0) -> dict:
-    """The oracle timed on this host's cores over a bounded sample of the step."""
+def cpu_baseline(wl, step_i: int, budget_s: float = 20.0, one_thread_s: float = 5.0) -> dict:
+    """The oracle timed on this host's cores over a bounded sample of the step.
+
+    Sample: every cross row, layers taken one at a time (each with the step's
+    append and selection) until `budget_s` is spent, on all host cores; then
+    rows of layer 0 one at a time on one thread until `one_thread_s` is spent."""
+    import oracle
     step = wl.steps[step_i]
     acc = accounting(wl, step)
     nthreads = host_cores()
     Ks, Vs = _oracle_setup(wl, step)
     kp, vp = wl.empty_pool(), wl.empty_pool()
     kv_lens = cross_rows_kv_lens(step)
-    # sample: all rows, layers taken one at a time until the budget is spent
     t0 = time.perf_counter()
     done = 0
     for layer in range(wl.layers):
@@ -538,11 +641,43 @@ def cpu_baseline(wl, step_i: int, budget_s: float = 20.0) -> dict:
             break
     dt = time.perf_counter() - t0
     kv_bytes = acc["kv_bytes_layer"] * done
+    per_key = 2 * wl.num_kv_heads * wl.head_dim * (4 if wl.dtype == "f32" else 2)
+    _, cqsl, _ = oracle.select_cross_rows(step.query_start_loc, step.rows_per_req)
+    q0 = oracle.widen(step.q[0], wl.dtype)
+    t1 = time.perf_counter()
+    rows1 = 0
+    bytes1 = 0
+    for n in range(int(kv_lens.shape[0])):
+        oracle.cross_attn(q0, Ks, Vs, step.seq_lens, cqsl, wl.scale, rows=[n], nthreads=1)
+        rows1 += 1
+        bytes1 += int(kv_lens[n]) * per_key
+        if time.perf_counter() - t1 > one_thread_s:
+            break
+    dt1 = time.perf_counter() - t1
     return {"value": round(kv_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": nthreads,
             "kind": "oracle",
             "sample": f"{acc['rows']} rows x {done} of {wl.layers} layers of {wl.name} "
                       f"(sum kv_len {int(kv_lens.sum())}), float64, {dt:.1f} s",
-            "query_rows_per_s": round(acc["rows"] * done / dt, 3)}
+            "query_rows_per_s": round(acc["rows"] * done / dt, 3),
+            "one_thread": {"value": round(bytes1 / dt1 / 1e9, 4), "unit": "GB/s", "cores": 1,
+                           "query_rows_per_s": round(rows1 / dt1, 3),
+                           "sample": f"{rows1} rows of layer 0, attention only, {dt1:.1f} s"}}
+
+
+def workload_config(wl, step, acc, world, fused=False, workload_name=None) -> dict:
+    """The `config` dict of a bench line (both arms print it for the same workload)."""
+    return {
+        "workload": workload_name or wl.name, "description": wl.description,
+        "H_q": wl.num_q_heads, "H_kv": wl.num_kv_heads, "head_dim": wl.head_dim,
+        "block_size": wl.block_size, "layers": wl.layers, "requests": step.num_reqs,
+        "step_tokens": step.num_tokens, "cross_rows": acc["rows"],
+        "kv_bytes_per_layer": acc["kv_bytes_layer"],
+        "l2": ("inputs larger than L2" if acc["kv_bytes_layer"] > 129e6
+               else "inputs fit in L2 (layers re-read them: logical bytes)"),
+        "parallelism": f"replicas x{world}",
+        "step": ("append fused into layer 0 (yoco_cross_decode_step)" if fused
+                 else "append, select, every layer"),
+    }
 
 
 def run_reference(args, rank, world):
@@ -575,7 +710,7 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
-        "config": {"workload": wl.name, "description": wl.description},
+        "config": workload_config(wl, step, acc, world),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": nthreads,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,

@@ -79,7 +79,8 @@ typedef enum { YOCO_F32 = 0, YOCO_BF16 = 1, YOCO_E4M3 = 2 } yoco_dtype_t;
 
 /* Bits OR-ed into *err_word by device code. */
 #define YOCO_DEVERR_PAGE_RANGE 0x1   /* block_table entry outside [0, num_blocks) */
-#define YOCO_DEVERR_POS_RANGE 0x2    /* position beyond max_blocks_per_req * block_size, or negative */
+#define YOCO_DEVERR_POS_RANGE 0x2    /* position beyond max_blocks_per_req * block_size, or negative;
+                                        attention: a row with more keys than max_seq_len */
 #define YOCO_DEVERR_EMPTY_ROW 0x4    /* a cross row with no key to attend (seq_len < rows of its request) */
 #define YOCO_DEVERR_OFFSETS 0x8      /* query_start_loc decreasing, or rows_per_req negative */
 #define YOCO_DEVERR_TIMEOUT 0x10     /* a bounded wait on an asynchronous copy gave up */
@@ -161,7 +162,12 @@ size_t yoco_cross_attn_workspace_size(int32_t max_rows, int32_t num_q_heads, int
  *   block_table, seq_lens  device int32, as for yoco_kv_append
  *   cross_query_start_loc  device int32 [num_reqs + 1] (from yoco_select_cross_rows)
  *   max_rows               host bound on the number of rows (grid size)
- *   max_seq_len            host bound on seq_lens (sizes the split-KV grid)
+ *   max_seq_len            host bound on seq_lens (sizes the fp32 split-KV grid and its
+ *                          workspace). A row with more keys sets YOCO_DEVERR_POS_RANGE; the
+ *                          fp32 path then attends only to its first max_seq_len keys, so no
+ *                          scratch beyond the workspace is ever touched (the bf16 path,
+ *                          whose scratch does not depend on context length, attends to all
+ *                          of them)
  *   scale                  softmax scale (1/sqrt(head_dim) for the pages' definition)
  *   flags                  bits of YOCO_ATTN_REVERSE | YOCO_ATTN_OVERLAP | YOCO_ATTN_KEEP_TAIL
  *                          (other bits are rejected; all are ignored on the fp32 path).
@@ -315,9 +321,16 @@ yoco_status_t yoco_cross_decode_step(const void* q, const void* k_new, const voi
  *   - Returns YOCO_ERR_WORKSPACE, before any launch, when these bounds need
  *     more scratch than the array holds (yoco_cross_attn_workspace_size()
  *     gives the need).
+ *   - dtype YOCO_F32 or YOCO_BF16 only: YOCO_E4M3 (and any other value)
+ *     returns YOCO_ERR_UNSUPPORTED before any launch. No flags are taken:
+ *     the call runs as yoco_cross_attn_paged with flags 0 (no REVERSE,
+ *     OVERLAP or KEEP_TAIL).
  *   - The first call on each device looks up the array's device address
  *     (with that device current); make that first call before any stream
- *     capture on the device.
+ *     capture on the device. The address is kept for the life of the
+ *     process: it assumes the device's primary context is never reset
+ *     (no cudaDeviceReset between calls), since a reset reloads the module
+ *     and moves the array.
  *   - Every call on a device shares the one array. The library writes each
  *     scratch word before reading it within a call, so no clearing is
  *     needed, but calls that overlap on the GPU (other streams, other host
@@ -347,6 +360,9 @@ size_t yoco_cross_attn_noalloc_capacity(void);
  * is the fraction of its lines given the persisting property, and a
  * negative hit_ratio means "as many as the set-aside holds" (set-aside /
  * window), so that the same lines stay resident from one layer to the next.
+ * Clearing the window (bytes == 0) also resets the lines already marked
+ * persisting to normal (cudaCtxResetPersistingL2Cache) and the context's
+ * persisting set-aside to zero, so that later kernels get the whole L2 back.
  */
 yoco_status_t yoco_set_l2_window(void* stream, void* base, size_t bytes, float hit_ratio);
 

@@ -60,3 +60,14 @@ def test_replicas_have_the_same_shapes_and_their_own_data(config):
     assert sa.q[0].shape == sb.q[0].shape
     assert sa.k_new.shape[1:] == sb.k_new.shape[1:]
     assert not (sa.q[0] == sb.q[0]).all()
+
+
+def test_reference_config_matches_the_gpu_arm(capsys, monkeypatch):
+    """Both arms print the same `config` for the same workload, so the driver can pair them."""
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    out = _run(capsys, ["--impl", "reference", "--config", "0", "--steps", "1", "--warmup", "0"])
+    d = json.loads(out[0])
+    wl = bench.make_workload(0)
+    st = wl.steps[-1]
+    assert d["config"] == bench.workload_config(wl, st, bench.accounting(wl, st), 1)

@@ -348,3 +348,44 @@ def test_chunked_prefill_and_speculative_rows(P):
         assert np.abs(got - ref).max() <= ATOL["bf16"], i
     kp, vp = oracle_pools(wl)
     assert np.array_equal(pool_bits(dw.k_cache), oracle_bits(kp))
+
+
+@pytest.mark.parametrize("max_seq_len", [300, 1000])
+def test_fp32_rows_beyond_max_seq_len_are_cut_and_flagged(P, N, max_seq_len):
+    """fp32 split-KV path: a seq_len above the caller's max_seq_len bound.
+
+    The split plan and its workspace are sized for max_seq_len keys per row
+    (none at all when one split suffices), so the kernels cut such a row to
+    its first max_seq_len keys and set POS_RANGE; nothing outside `out` and
+    the workspace is written (canaries on both sides of each)."""
+    import dataclasses
+    lens = [150, 2000, 3000, 40]
+    wl = pure_decode(3400 + max_seq_len, explicit_lens=lens, H_q=8, H_kv=2, D=128, bs=16,
+                     layers=1, dtype="f32")
+    dw = P.DeviceWorkload(wl)
+    dw.run_fill()
+    dw.run_step(0)  # append + select (+ layer 0 with the true bound)
+    torch.cuda.synchronize()
+    assert dw.error_bits() == 0
+    ds = dw.steps[0]
+    need = N.yoco_cross_attn_workspace_size(ds.rows_upper, wl.num_q_heads, wl.num_kv_heads,
+                                            wl.head_dim, wl.block_size, max_seq_len,
+                                            torch.float32)
+    pad = 4096
+    wsb = torch.full((pad + max(need, 16) + pad,), 0x5A, dtype=torch.uint8, device="cuda")
+    ws = wsb[pad:pad + need] if need > 0 else None
+    n_out = ds.out[0].numel()
+    big = torch.full((pad + n_out + pad,), 7.0, dtype=torch.float32, device="cuda")
+    out = big[pad:pad + n_out].view(ds.out[0].shape)
+    dw.err.zero_()
+    N.yoco_cross_attn_paged(ds.dev["q"][0], dw.k_cache, dw.v_cache, out, ds.dev["block_table"],
+                            ds.dev["seq_lens"], ds.cqsl, max_seq_len, wl.scale, ws, dw.err)
+    torch.cuda.synchronize()
+    assert dw.error_bits() == N.DEVERR_POS_RANGE
+    assert (big[:pad] == 7.0).all() and (big[pad + n_out:] == 7.0).all()
+    assert (wsb[:pad] == 0x5A).all() and (wsb[pad + need:] == 0x5A).all()
+    got = gpu_out(out)[None]
+    assert np.isfinite(got).all()
+    cut = dataclasses.replace(wl.steps[0], seq_lens=np.minimum(wl.steps[0].seq_lens, max_seq_len))
+    ref = oracle_step_out(wl, cut)
+    assert np.abs(got - ref).max() <= ATOL["f32"]

@@ -15,7 +15,7 @@ import numpy as np
 import pytest
 import torch
 
-from tests.helpers import ATOL, gpu_out
+from tests.helpers import ATOL, gpu_out, oracle_step_out
 from workloads import SMALL
 
 pytestmark = pytest.mark.gpu
@@ -61,16 +61,30 @@ def test_noalloc_matches_workspace_entry_point(idx):
                                             wl.head_dim, wl.block_size, ds.max_seq_len,
                                             P.torch_dtype(wl.dtype))
     assert need <= N.yoco_cross_attn_noalloc_capacity()
+    # the workspace entry with the flags the allocation-free entry uses (none):
+    # the same kernels on the same inputs in the same order, so bit-identical
+    refs = {}
+    for layer in (0, wl.layers - 1):
+        refs[layer] = torch.full_like(ds.out[layer], float("nan"))
+        N.yoco_cross_attn_paged(ds.dev["q"][layer], dw.k_cache, dw.v_cache, refs[layer],
+                                ds.dev["block_table"], ds.dev["seq_lens"], ds.cqsl,
+                                ds.max_seq_len, wl.scale, ds.workspace, dw.err, flags=0)
+    torch.cuda.synchronize()
+    assert dw.error_bits() == 0
+    oracle_ref = oracle_step_out(wl, wl.steps[i], layers=[0])[0]
     for call in range(2):  # two calls in a row share the one scratch array
         for layer in (0, wl.layers - 1):
             out = torch.full_like(ds.out[layer], float("nan"))
             assert _call_noalloc(N, dw, ds, layer, out) == N.YOCO_OK
             torch.cuda.synchronize()
             assert dw.error_bits() == 0
-            ref = gpu_out(ds.out[layer])
             got = gpu_out(out)
             assert np.isfinite(got).all()
-            assert np.abs(got - ref).max() <= ATOL[wl.dtype], (idx, call, layer)
+            assert torch.equal(out, refs[layer]), (idx, call, layer)
+            # and the regular pipeline (its own flags) within tolerance
+            assert np.abs(got - gpu_out(ds.out[layer])).max() <= ATOL[wl.dtype]
+            if layer == 0:  # one layer straight against the oracle
+                assert np.abs(got - oracle_ref).max() <= ATOL[wl.dtype], (idx, call)
 
 
 def test_noalloc_rejects_bounds_beyond_its_array():

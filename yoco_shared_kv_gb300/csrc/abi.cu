@@ -45,6 +45,10 @@ extern "C" yoco_status_t yoco_set_l2_window(void* stream, void* base, size_t byt
         attr.accessPolicyWindow.hitProp = cudaAccessPropertyNormal;
         attr.accessPolicyWindow.missProp = cudaAccessPropertyNormal;
         YOCO_CUDA_OK(cudaStreamSetAttribute(s, cudaStreamAttributeAccessPolicyWindow, &attr));
+        // lines already marked persisting would otherwise keep their set-aside,
+        // and the set-aside itself (this context's only) goes back to none
+        YOCO_CUDA_OK(cudaCtxResetPersistingL2Cache());
+        YOCO_CUDA_OK(cudaDeviceSetLimit(cudaLimitPersistingL2CacheSize, 0));
         return YOCO_OK;
     }
     if (!(hit_ratio <= 1.f)) return YOCO_ERR_INVALID_ARG;  // negative: automatic

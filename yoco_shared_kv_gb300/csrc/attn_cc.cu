@@ -13,6 +13,13 @@
 namespace yoco {
 namespace {
 
+// Keys a row may attend on this path: the block table's reach and the
+// caller's max_seq_len, whichever is smaller.
+__device__ __forceinline__ int32_t row_key_cap(const AttnParams& p) {
+    const int64_t bt = static_cast<int64_t>(p.max_blocks) * p.block_size;
+    return static_cast<int32_t>(bt < p.max_seq_len ? bt : p.max_seq_len);
+}
+
 // Resolve a CTA's row / split. Returns false if the CTA has no work.
 // On an empty row the split-0 CTA zero-fills `heads` output heads starting
 // at `head0` and flags the error.
@@ -29,13 +36,17 @@ __device__ __forceinline__ bool cta_range(const AttnParams& p, int32_t n, int32_
         }
         return false;
     }
-    const int64_t cap = static_cast<int64_t>(p.max_blocks) * p.block_size;
+    // The split plan (and the workspace) hold max_seq_len keys per row: a row
+    // with more (seq_lens above the caller's bound) is cut to that many and
+    // flagged, so that no split slot past max_splits is ever written or read.
+    const int32_t cap = row_key_cap(p);
     if (kv_len > cap) {
         if (threadIdx.x == 0 && s == 0) set_err(p.err, YOCO_DEVERR_POS_RANGE);
-        kv_len = static_cast<int32_t>(cap);
+        kv_len = cap;
     }
     const int32_t n_pages = (kv_len + p.block_size - 1) / p.block_size;
     nsplit = (n_pages + p.split_pages - 1) / p.split_pages;
+    if (nsplit > p.max_splits) nsplit = p.max_splits;  // unreachable after the cut; kept as a bound
     if (s >= nsplit) return false;
     p_begin = s * p.split_pages;
     p_end = min(n_pages, p_begin + p.split_pages);
@@ -161,10 +172,11 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_cc(const AttnParams 
     const int32_t n = blockIdx.x, h = blockIdx.y;
     int32_t req, kv_len;
     if (!locate_row(p.cqsl, p.num_reqs, n, p.seq_lens, req, kv_len) || kv_len <= 0) return;
-    const int64_t cap = static_cast<int64_t>(p.max_blocks) * p.block_size;
-    if (kv_len > cap) kv_len = static_cast<int32_t>(cap);
+    const int32_t cap = row_key_cap(p);  // the same cut as the split kernel's
+    if (kv_len > cap) kv_len = cap;
     const int32_t n_pages = (kv_len + p.block_size - 1) / p.block_size;
-    const int32_t nsplit = (n_pages + p.split_pages - 1) / p.split_pages;
+    int32_t nsplit = (n_pages + p.split_pages - 1) / p.split_pages;
+    if (nsplit > p.max_splits) nsplit = p.max_splits;
     if (nsplit <= 1) return;
     const int64_t head = static_cast<int64_t>(n) * p.H_q + h;
     const float2* ml = p.ws_ml + head * p.max_splits;

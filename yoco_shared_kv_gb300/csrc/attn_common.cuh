@@ -30,6 +30,7 @@ struct AttnParams {
     int32_t block_size;
     int32_t split_pages;        // CUDA-core path: logical pages per split
     int32_t max_splits;         // CUDA-core path
+    int32_t max_seq_len;        // host bound on seq_lens (the CUDA-core split plan is sized by it)
     const float4* scales;       // e4m3 cache: {k_scale, v_scale, -, -} per (page, kv head)
     float scale_log2;           // softmax scale * log2(e)
     int32_t reverse;            // tensor-core path: walk each worker's pages from the end

@@ -476,7 +476,7 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
                     for (int i = lane; i < p.H_q * D; i += 32)
                         outz[static_cast<int64_t>(n) * p.H_q * D + i] = __float2bfloat16_rn(0.f);
                     if (lane == 0) set_err(p.err, YOCO_DEVERR_EMPTY_ROW);
-                } else if (kv > cap && lane == 0) {
+                } else if ((kv > cap || kv > p.max_seq_len) && lane == 0) {
                     set_err(p.err, YOCO_DEVERR_POS_RANGE);
                 }
             }

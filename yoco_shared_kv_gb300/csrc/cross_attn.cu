@@ -222,6 +222,7 @@ yoco_status_t run_attn(const void* q, const void* k_cache, const void* v_cache,
     p.block_size = block_size;
     p.split_pages = pl.split_pages;
     p.max_splits = pl.max_splits;
+    p.max_seq_len = max_seq_len;
     p.scales = reinterpret_cast<const float4*>(page_scales);
     p.scale_log2 = scale * kLog2e;
     p.reverse = (flags & YOCO_ATTN_REVERSE) ? 1 : 0;
