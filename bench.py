@@ -269,12 +269,12 @@ def cold_layer_ms(dw, ds, cq, stream, dev, reps):
     import torch
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.zeros(2 * l2 // 4, dtype=torch.int32, device=dev)
-    sink = torch.zeros(1, dtype=torch.int64, device=dev)
+    sink = torch.zeros((), dtype=torch.int64, device=dev)
     out = {}
     for kind in ("clean", "dirty"):
         def fl():
             if kind == "clean":
-                torch.sum(flush, out=sink)
+                torch.sum(flush, dim=0, out=sink)
             else:
                 flush.zero_()
         g_fl, g_cold = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
@@ -341,12 +341,14 @@ def measure(args, config, rank, world, local, *, kv="native", fused=False, steps
             dw.run_step(i, stream)
     stream.synchronize()
 
-    merges = 1 if N.yoco_cross_attn_workspace_size(max(ds.rows_upper, 1), wl.num_q_heads,
-                                                   wl.num_kv_heads, wl.head_dim, wl.block_size,
-                                                   ds.max_seq_len,
-                                                   torch.float8_e4m3fn if e4m3
-                                                   else P.torch_dtype(wl.dtype)) > 0 else 0
-    launches_per_step = (0 if fused else 2) + wl.layers * (1 + merges)
+    # our kernels per step: append and selection (unless fused), the step's
+    # plan (tensor-core paths), and per layer one attention kernel (the fp32
+    # path adds its split merge when the plan has more than one split)
+    tc = e4m3 or wl.dtype == "bf16"
+    merges = 0 if tc else (1 if N.yoco_cross_attn_workspace_size(
+        max(ds.rows_upper, 1), wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.block_size,
+        ds.max_seq_len, P.torch_dtype(wl.dtype)) > 0 else 0)
+    launches_per_step = (0 if fused else 2) + (1 if tc else 0) + wl.layers * (1 + merges)
 
     L = wl.layers
     # The step runs as one CUDA graph (append -> select -> every layer), as an
@@ -478,7 +480,7 @@ def measure(args, config, rank, world, local, *, kv="native", fused=False, steps
         "config": workload_config(wl, wl.steps[step_i], acc, world, fused, workload_name),
         "hbm_frac": round(value / peak, 4),
         "query_rows_per_s": round(total_rows / (max_ms / 1e3), 1),
-        "roofline": {"kernel": DOMINANT_KERNEL + " (+ split merge)", "bound": "hbm",
+        "roofline": {"kernel": DOMINANT_KERNEL + " (cross-CTA merge inside)", "bound": "hbm",
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      # DRAM-side fraction: the bytes DRAM actually moved per launch

@@ -76,6 +76,7 @@ typedef enum { YOCO_F32 = 0, YOCO_BF16 = 1, YOCO_E4M3 = 2 } yoco_dtype_t;
 #define YOCO_ATTN_REVERSE 0x1u /* tensor-core paths: walk each worker's pages last to first */
 #define YOCO_ATTN_OVERLAP 0x2u /* tensor-core paths: may start while the previous kernel drains */
 #define YOCO_ATTN_KEEP_TAIL 0x4u /* tensor-core paths: L2 hints that keep this walk's tail for the next layer */
+#define YOCO_ATTN_PLANNED 0x8u /* tensor-core paths: the workspace holds this step's plan (yoco_cross_attn_plan) */
 
 /* Bits OR-ed into *err_word by device code. */
 #define YOCO_DEVERR_PAGE_RANGE 0x1   /* block_table entry outside [0, num_blocks) */
@@ -85,6 +86,7 @@ typedef enum { YOCO_F32 = 0, YOCO_BF16 = 1, YOCO_E4M3 = 2 } yoco_dtype_t;
 #define YOCO_DEVERR_OFFSETS 0x8      /* query_start_loc decreasing, or rows_per_req negative */
 #define YOCO_DEVERR_TIMEOUT 0x10     /* a bounded wait on an asynchronous copy gave up */
 #define YOCO_DEVERR_SCALE 0x20       /* e4m3 cache: a page scale outside the supported range */
+#define YOCO_DEVERR_PLAN 0x40        /* YOCO_ATTN_PLANNED, but the workspace holds no plan for these shapes */
 
 /*
  * yoco_kv_append — write the step's new shared K^/V^ into the paged cache.
@@ -169,17 +171,25 @@ size_t yoco_cross_attn_workspace_size(int32_t max_rows, int32_t num_q_heads, int
  *                          whose scratch does not depend on context length, attends to all
  *                          of them)
  *   scale                  softmax scale (1/sqrt(head_dim) for the pages' definition)
- *   flags                  bits of YOCO_ATTN_REVERSE | YOCO_ATTN_OVERLAP | YOCO_ATTN_KEEP_TAIL
- *                          (other bits are rejected; all are ignored on the fp32 path).
+ *   flags                  bits of YOCO_ATTN_REVERSE | YOCO_ATTN_OVERLAP | YOCO_ATTN_KEEP_TAIL |
+ *                          YOCO_ATTN_PLANNED (other bits are rejected; all are ignored on the
+ *                          fp32 path).
+ *                          PLANNED: the workspace holds the plan that yoco_cross_attn_plan made
+ *                          for this step (same metadata arrays, unchanged since, and the same
+ *                          max_rows, shapes and dtype), so the call launches the attention
+ *                          kernel alone. Without it the call first makes that plan itself (one
+ *                          more small kernel). A plan made for other shapes is detected: the
+ *                          call then writes nothing and sets YOCO_DEVERR_PLAN.
  *                          REVERSE: the serial layers re-read one cache ("YOCO 论文与推理
  *                          数据流详解" §11); with the flag set on every other layer, a layer
  *                          starts on the pages the previous one read last, which are still
  *                          in L2. The result is the same up to summation order.
  *                          OVERLAP: the call is launched as a programmatic dependent of the
  *                          kernel before it on `stream`, so it reads block_table, seq_lens,
- *                          cross_query_start_loc and the cache while that kernel drains.
- *                          Set it only when that kernel writes none of those (for example
- *                          the previous cross-decoder layer); queries, outputs and the
+ *                          cross_query_start_loc, the cache and (with PLANNED) the plan while
+ *                          that kernel drains. Set it only when that kernel writes none of
+ *                          those (for example the previous cross-decoder layer, but not
+ *                          yoco_cross_attn_plan); queries, outputs and the rest of the
  *                          workspace are touched only after that kernel has finished.
  *                          KEEP_TAIL: the pages are copied with an L2 evict-first hint except
  *                          the last ones each worker reads (evict-last, about 40 MB for a
@@ -187,12 +197,19 @@ size_t yoco_cross_attn_workspace_size(int32_t max_rows, int32_t num_q_heads, int
  *                          layer; meant for layers that alternate YOCO_ATTN_REVERSE over a
  *                          cache larger than L2. Hints only: the result is unchanged.
  *   workspace              device scratch of >= yoco_cross_attn_workspace_size(...) bytes,
- *                          16-byte aligned; contents need no initialisation
+ *                          16-byte aligned; contents need no initialisation (the plan is
+ *                          written into it by yoco_cross_attn_plan or by a call without
+ *                          PLANNED). One workspace serves one stream at a time.
  *   err_word               device int32 or NULL
  * Long contexts are split across CTAs and merged with a log-sum-exp
  * combine in a fixed split order, so results do not depend on where pages
  * sit in the pool. Accuracy: fp32 accumulation; bf16 probabilities feed the
  * tensor-core P.V product.
+ * The bf16 and e4m3 kernels run one CTA per SM, and the CTAs that share a
+ * context cut between them wait (bounded) for each other before combining
+ * it: every CTA of the grid must become resident. On a device whose SMs are
+ * partitioned below its SM count (MPS thread limits, green contexts) such a
+ * wait gives up after one second and sets YOCO_DEVERR_TIMEOUT.
  */
 yoco_status_t yoco_cross_attn_paged(const void* q, const void* k_cache, const void* v_cache,
                                     void* out, const int32_t* block_table,
@@ -203,6 +220,33 @@ yoco_status_t yoco_cross_attn_paged(const void* q, const void* k_cache, const vo
                                     int32_t num_blocks, float scale, yoco_dtype_t dtype,
                                     uint32_t flags, void* workspace, size_t workspace_bytes,
                                     int32_t* err_word, void* stream);
+
+/*
+ * yoco_cross_attn_plan — the per-step plan of the tensor-core attention.
+ *
+ * Every cross-decoder layer of a step attends with the same metadata to the
+ * one shared cache ("YOCO 论文与推理数据流详解" §10.4, §11), so the way its
+ * pages are dealt to the kernel's warps is the same for all of them. This
+ * call works it out once, into `workspace`: each warp's first page and the
+ * block-table entries of its first page copies, each CTA's first and last
+ * segment, and the CTAs' arrival counters. The layers then pass
+ * YOCO_ATTN_PLANNED and start streaming after one dependent load.
+ *   arguments    as for yoco_cross_attn_paged (the same values the layers will pass);
+ *                dtype YOCO_BF16 or YOCO_E4M3 (the e4m3 layers' own kernel shape);
+ *                YOCO_F32 needs no plan and returns YOCO_OK without a launch
+ *   flags        0 or YOCO_ATTN_OVERLAP (the previous kernel on `stream` writes none of
+ *                block_table, seq_lens, cross_query_start_loc; the plan is written after it
+ *                has finished)
+ * Call it after the metadata of the step is final (after yoco_select_cross_rows), and again
+ * whenever block_table, seq_lens, cross_query_start_loc or max_rows change.
+ */
+yoco_status_t yoco_cross_attn_plan(const int32_t* block_table, int32_t max_blocks_per_req,
+                                   const int32_t* seq_lens, const int32_t* cross_query_start_loc,
+                                   int32_t num_reqs, int32_t max_rows, int32_t max_seq_len,
+                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                   int32_t block_size, int32_t num_blocks, yoco_dtype_t dtype,
+                                   uint32_t flags, void* workspace, size_t workspace_bytes,
+                                   int32_t* err_word, void* stream);
 
 /*
  * 8-bit cache: e4m3 K^/V^ with a K and a V scale per (page, kv head)
@@ -289,10 +333,12 @@ yoco_status_t yoco_cross_attn_paged_e4m3(const void* q, const void* k_cache, con
  *   dtype             YOCO_BF16 (page_scales ignored) or YOCO_E4M3 (page_scales as for
  *                     yoco_kv_append_e4m3); the pools hold that format
  *   workspace         >= yoco_cross_attn_workspace_size(num_reqs, ..., dtype) bytes
- * Other arguments, checks and errors are those of yoco_cross_attn_paged; of the flags only
- * YOCO_ATTN_OVERLAP is taken (YOCO_ATTN_REVERSE is rejected: the step walks its pages
- * forward). The cache ends bit-identical to the separate append, and the output to the
- * separate attention.
+ * Other arguments, checks and errors are those of yoco_cross_attn_paged; of the flags
+ * YOCO_ATTN_OVERLAP, YOCO_ATTN_KEEP_TAIL and YOCO_ATTN_PLANNED are taken (YOCO_ATTN_REVERSE
+ * is rejected: the step walks its pages forward). Without PLANNED the call makes the
+ * step's plan (query_start_loc as the cross query_start_loc), which the later layers of
+ * the step can reuse with YOCO_ATTN_PLANNED. The cache ends bit-identical to the separate
+ * append, and the output to the separate attention.
  */
 yoco_status_t yoco_cross_decode_step(const void* q, const void* k_new, const void* v_new,
                                      void* k_cache, void* v_cache, const float* page_scales,
@@ -324,7 +370,8 @@ yoco_status_t yoco_cross_decode_step(const void* q, const void* k_new, const voi
  *   - dtype YOCO_F32 or YOCO_BF16 only: YOCO_E4M3 (and any other value)
  *     returns YOCO_ERR_UNSUPPORTED before any launch. No flags are taken:
  *     the call runs as yoco_cross_attn_paged with flags 0 (no REVERSE,
- *     OVERLAP or KEEP_TAIL).
+ *     OVERLAP, KEEP_TAIL or PLANNED), so each call makes its own plan in
+ *     the array before its attention launch.
  *   - The first call on each device looks up the array's device address
  *     (with that device current); make that first call before any stream
  *     capture on the device. The address is kept for the life of the

@@ -74,7 +74,7 @@ def test_host_validation_rejects_before_launch(lib_path):
     assert call(hq=34, hkv=2) == 2  # group of 17
     assert call(dt=5) == 2          # unknown dtype
     assert call() == 1              # null pointers
-    assert call(flags=0x8) == 1     # unknown flag bit
+    assert call(flags=0x10) == 1    # unknown flag bit
     L.yoco_select_cross_rows.restype = ctypes.c_int
     L.yoco_select_cross_rows.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp]
     assert L.yoco_select_cross_rows(None, None, -1, None, None, None, None, None) == 1
@@ -110,7 +110,7 @@ def test_e4m3_host_validation(lib_path):
     assert attn(bs=8) == N.YOCO_ERR_UNSUPPORTED
     assert attn(sc=None) == N.YOCO_ERR_INVALID_ARG  # scale records are required
     assert attn(sc=fake + 8) == N.YOCO_ERR_INVALID_ARG  # 16-byte records, 16-byte aligned
-    assert attn(flags=0x8) == N.YOCO_ERR_INVALID_ARG
+    assert attn(flags=0x10) == N.YOCO_ERR_INVALID_ARG  # unknown flag bit
     assert attn() == N.YOCO_ERR_WORKSPACE           # no workspace given
     # the bf16 entry refuses the e4m3 dtype
     assert L.yoco_cross_attn_paged(fake, fake, fake, fake, fake, 4, fake, fake, 1, 1, 64, 8, 2,
@@ -218,3 +218,29 @@ def test_noalloc_and_l2_window_host_validation(lib_path):
                                      ctypes.c_float]
     assert L.yoco_set_l2_window(None, fake, 1 << 20, 1.5) == N.YOCO_ERR_INVALID_ARG
     assert L.yoco_set_l2_window(None, fake, 1 << 20, float("nan")) == N.YOCO_ERR_INVALID_ARG
+
+
+def test_plan_host_validation(lib_path):
+    """yoco_cross_attn_plan checks its arguments before any launch; the fp32
+    path plans on the host and returns without one."""
+    import torch
+    from yoco_shared_kv_gb300 import _native as N
+    L = N.lib
+    fake = 1 << 20  # never dereferenced: every call below returns before a launch
+
+    def plan(dt=N.YOCO_BF16, d=128, bs=32, flags=0, ws=fake, ws_bytes=None, bt=fake, hq=16, hkv=1):
+        need = N.yoco_cross_attn_workspace_size(4, hq, hkv, d, bs, 4096,
+                                                {N.YOCO_BF16: torch.bfloat16,
+                                                 N.YOCO_F32: torch.float32}.get(dt, torch.uint8))
+        return L.yoco_cross_attn_plan(bt, 128, fake, fake, 4, 4, 4096, hq, hkv, d, bs, 1000, dt,
+                                      flags, ws, need if ws_bytes is None else ws_bytes, None, None)
+    assert plan(flags=N.YOCO_ATTN_REVERSE) == N.YOCO_ERR_INVALID_ARG   # only OVERLAP is taken
+    assert plan(flags=N.YOCO_ATTN_PLANNED) == N.YOCO_ERR_INVALID_ARG
+    assert plan(bt=None) == N.YOCO_ERR_INVALID_ARG
+    assert plan(ws=fake + 8) == N.YOCO_ERR_INVALID_ARG                # 16-byte aligned workspace
+    assert plan(ws_bytes=16) == N.YOCO_ERR_WORKSPACE
+    assert plan(ws=None) == N.YOCO_ERR_WORKSPACE
+    assert plan(d=96) == N.YOCO_ERR_UNSUPPORTED
+    assert plan(dt=N.YOCO_E4M3, d=64) == N.YOCO_ERR_UNSUPPORTED      # e4m3 pages need 128-byte rows
+    assert plan(hq=17, hkv=1) == N.YOCO_ERR_UNSUPPORTED
+    assert plan(dt=N.YOCO_F32, ws=None, ws_bytes=0, hq=8, hkv=2) == N.YOCO_OK  # no plan needed

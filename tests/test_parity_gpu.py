@@ -300,6 +300,7 @@ def test_attention_writes_only_its_outputs(P, N, lens, H_q, H_kv, D, bs):
     big = torch.full((pad + n_out + pad,), 7.0, dtype=torch.bfloat16, device="cuda")
     out = big[pad:pad + n_out].view(ds.out[0].shape)
     ds.workspace.fill_(255)
+    dw.plan(ds)  # the step's plan, then every other scratch byte is still NaN
     dw.attend(ds, 0, out=out)
     torch.cuda.synchronize()
     assert dw.error_bits() == 0
@@ -389,3 +390,87 @@ def test_fp32_rows_beyond_max_seq_len_are_cut_and_flagged(P, N, max_seq_len):
     cut = dataclasses.replace(wl.steps[0], seq_lens=np.minimum(wl.steps[0].seq_lens, max_seq_len))
     ref = oracle_step_out(wl, cut)
     assert np.abs(got - ref).max() <= ATOL["f32"]
+
+
+@pytest.mark.parametrize("idx", [1, 2, 3, 4])
+def test_planned_layers_equal_unplanned_calls(P, N, idx):
+    """A layer reusing the step's plan (YOCO_ATTN_PLANNED) gives the same bits as
+    a self-contained call that makes its own plan first, for both page walks."""
+    wl = SMALL[idx]()
+    dw = P.DeviceWorkload(wl, alternate=True)
+    dw.run_all()
+    torch.cuda.synchronize()
+    assert dw.error_bits() == 0
+    ds = dw.steps[-1]
+    for layer in range(wl.layers):
+        flags = N.YOCO_ATTN_KEEP_TAIL | (N.YOCO_ATTN_REVERSE if layer % 2 else 0)
+        out = torch.full_like(ds.out[layer], float("nan"))
+        N.yoco_cross_attn_paged(ds.dev["q"][layer], dw.k_cache, dw.v_cache, out,
+                                ds.dev["block_table"], ds.dev["seq_lens"], ds.cqsl,
+                                ds.max_seq_len, wl.scale, ds.workspace, dw.err, flags=flags)
+        torch.cuda.synchronize()
+        assert dw.error_bits() == 0
+        assert torch.equal(out.view(torch.int16), ds.out[layer].view(torch.int16)), layer
+    ref = oracle_step_out(wl, wl.steps[-1])
+    assert np.abs(gpu_out(ds.out) - ref).max() <= ATOL["bf16"]
+
+
+def test_planned_call_without_a_matching_plan_is_refused(P, N):
+    """YOCO_ATTN_PLANNED on a workspace that holds no plan, or a plan made for
+    other shapes: the launch writes nothing and sets YOCO_DEVERR_PLAN."""
+    wl = SMALL[1]()
+    dw = P.DeviceWorkload(wl)
+    dw.run_all()
+    torch.cuda.synchronize()
+    ds = dw.steps[0]
+    q = ds.dev["q"][0]
+    args = (dw.k_cache, dw.v_cache)
+    # no plan at all (scratch bytes all ones)
+    ds.workspace.fill_(255)
+    out = torch.full_like(ds.out[0], 5.0)
+    dw.err.zero_()
+    N.yoco_cross_attn_paged(q, *args, out, ds.dev["block_table"], ds.dev["seq_lens"], ds.cqsl,
+                            ds.max_seq_len, wl.scale, ds.workspace, dw.err,
+                            flags=N.YOCO_ATTN_PLANNED)
+    torch.cuda.synchronize()
+    assert dw.error_bits() == N.DEVERR_PLAN
+    assert (out == 5.0).all()
+    # a plan made for fewer rows than the call asks for
+    rows = q.shape[0]
+    N.yoco_cross_attn_plan(ds.dev["block_table"], ds.dev["seq_lens"], ds.cqsl, ds.max_seq_len,
+                           rows - 1, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.block_size,
+                           dw.k_cache.shape[0], torch.bfloat16, ds.workspace, dw.err)
+    dw.err.zero_()
+    N.yoco_cross_attn_paged(q, *args, out, ds.dev["block_table"], ds.dev["seq_lens"], ds.cqsl,
+                            ds.max_seq_len, wl.scale, ds.workspace, dw.err,
+                            flags=N.YOCO_ATTN_PLANNED)
+    torch.cuda.synchronize()
+    assert dw.error_bits() == N.DEVERR_PLAN
+    assert (out == 5.0).all()
+    # the matching plan: accepted, and the result is the step's
+    dw.plan(ds)
+    dw.err.zero_()
+    N.yoco_cross_attn_paged(q, *args, out, ds.dev["block_table"], ds.dev["seq_lens"], ds.cqsl,
+                            ds.max_seq_len, wl.scale, ds.workspace, dw.err,
+                            flags=N.YOCO_ATTN_PLANNED)
+    torch.cuda.synchronize()
+    assert dw.error_bits() == 0
+    ref = oracle_step_out(wl, wl.steps[0], layers=[0])[0]
+    assert np.abs(gpu_out(out) - ref).max() <= ATOL["bf16"]
+
+
+def test_plan_is_reused_across_layers_and_replaced_per_step(P):
+    """The chunked-prefill / speculative schedule: three steps with different
+    metadata, each planned once and attended by every layer."""
+    from workloads import chunked_prefill_spec
+    wl = chunked_prefill_spec()
+    dw = P.DeviceWorkload(wl)
+    dw.run_fill()
+    for i, step in enumerate(wl.steps):
+        dw.run_step(i)
+        torch.cuda.synchronize()
+        assert dw.error_bits() == 0
+        n = int(dw.steps[i].num_rows.item())
+        got = gpu_out(dw.steps[i].out[:, :n])
+        ref = oracle_step_out(wl, step)
+        assert np.abs(got - ref).max() <= ATOL["bf16"], i

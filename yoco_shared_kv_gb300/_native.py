@@ -22,19 +22,21 @@ YOCO_F32, YOCO_BF16, YOCO_E4M3 = 0, 1, 2
 YOCO_ATTN_REVERSE = 0x1
 YOCO_ATTN_OVERLAP = 0x2
 YOCO_ATTN_KEEP_TAIL = 0x4
+YOCO_ATTN_PLANNED = 0x8
 DEVERR_PAGE_RANGE = 0x1
 DEVERR_POS_RANGE = 0x2
 DEVERR_EMPTY_ROW = 0x4
 DEVERR_OFFSETS = 0x8
 DEVERR_TIMEOUT = 0x10
 DEVERR_SCALE = 0x20
+DEVERR_PLAN = 0x40
 
 EXPORTED = ("yoco_kv_append", "yoco_select_cross_rows", "yoco_cross_attn_workspace_size",
             "yoco_cross_attn_paged", "yoco_set_l2_window", "yoco_status_string", "yoco_version",
             "yoco_last_cuda_error", "yoco_last_cuda_error_string",
             "yoco_cross_attn_paged_noalloc", "yoco_cross_attn_noalloc_capacity",
             "yoco_selftest_wait_timeout", "yoco_cross_decoder_bytes", "yoco_kv_append_e4m3",
-            "yoco_cross_attn_paged_e4m3", "yoco_cross_decode_step")
+            "yoco_cross_attn_paged_e4m3", "yoco_cross_decode_step", "yoco_cross_attn_plan")
 
 
 class YocoError(RuntimeError):
@@ -91,6 +93,9 @@ def _load() -> ctypes.CDLL:
     L.yoco_cross_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32,
                                          i32, i32, i32, i32, i32, ctypes.c_float, ctypes.c_int,
                                          ctypes.c_uint32, vp, sz, vp, vp]
+    L.yoco_cross_attn_plan.restype = ctypes.c_int
+    L.yoco_cross_attn_plan.argtypes = [vp, i32, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32,
+                                       ctypes.c_int, ctypes.c_uint32, vp, sz, vp, vp]
     L.yoco_cross_attn_paged_e4m3.restype = ctypes.c_int
     L.yoco_cross_attn_paged_e4m3.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32,
                                              i32, i32, i32, i32, i32, ctypes.c_float,
@@ -203,6 +208,23 @@ def yoco_cross_attn_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch
         _i32(cross_query_start_loc, "cross_query_start_loc"), R, max_rows, int(max_seq_len), H_q,
         H_kv, D, bs, num_blocks, float(scale), dtype_code(q.dtype), int(flags), _ptr(workspace),
         ws_bytes, None if err_word is None else _i32(err_word, "err_word"), _stream(stream)))
+
+
+def yoco_cross_attn_plan(block_table: torch.Tensor, seq_lens: torch.Tensor,
+                         cross_query_start_loc: torch.Tensor, max_seq_len: int, max_rows: int,
+                         num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
+                         num_blocks: int, dtype: torch.dtype, workspace: Optional[torch.Tensor],
+                         err_word: Optional[torch.Tensor] = None, stream=None,
+                         flags: int = 0) -> None:
+    """The step's plan into ``workspace``; later layers pass ``YOCO_ATTN_PLANNED``."""
+    R = cross_query_start_loc.shape[0] - 1
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("yoco_cross_attn_plan", lib.yoco_cross_attn_plan(
+        _i32(block_table, "block_table"), block_table.shape[1], _i32(seq_lens, "seq_lens"),
+        _i32(cross_query_start_loc, "cross_query_start_loc"), R, int(max_rows), int(max_seq_len),
+        int(num_q_heads), int(num_kv_heads), int(head_dim), int(block_size), int(num_blocks),
+        dtype_code(dtype), int(flags), _ptr(workspace), ws_bytes,
+        None if err_word is None else _i32(err_word, "err_word"), _stream(stream)))
 
 
 def yoco_cross_attn_paged_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,

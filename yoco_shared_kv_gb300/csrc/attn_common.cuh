@@ -36,6 +36,8 @@ struct AttnParams {
     int32_t reverse;            // tensor-core path: walk each worker's pages from the end
     int32_t overlap;            // tensor-core path: launch as a programmatic dependent
     int32_t keep_tail;          // tensor-core path: L2 hints, keep this walk's tail for the next layer
+    int32_t planned;            // tensor-core path: the workspace already holds this step's plan
+    int32_t plan_only;          // tensor-core path: make the plan, launch no attention
 };
 
 // Wait limit for one asynchronous page copy before a kernel gives up.

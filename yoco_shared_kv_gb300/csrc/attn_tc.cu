@@ -19,7 +19,7 @@ int nw_of(int D, int BS) {
 
 }  // namespace
 
-int tc_ctas(int sms) { return sms < kMaxMergePieces ? sms : kMaxMergePieces; }
+int tc_ctas(int sms) { return sms < kMaxCtas ? sms : kMaxCtas; }
 
 size_t tc_workspace_bytes(int sms, int H_kv, int G, int D, int BS, bool e4m3) {
     (void)H_kv;
@@ -28,7 +28,7 @@ size_t tc_workspace_bytes(int sms, int H_kv, int G, int D, int BS, bool e4m3) {
     const int nw = e4m3 ? (wide ? nw_of<true, 2>(D, BS) : nw_of<true, 1>(D, BS))
                         : (wide ? nw_of<false, 2>(D, BS) : nw_of<false, 1>(D, BS));
     const size_t pieces = static_cast<size_t>(tc_pieces(ctas, nw, G));
-    return pieces * (static_cast<size_t>(D) * 4 + 8) + static_cast<size_t>(ctas) * sizeof(CtaHdr);
+    return static_cast<size_t>(tc_plan_bytes(ctas, nw)) + pieces * (static_cast<size_t>(D) * 4 + 8);
 }
 
 cudaError_t launch_attn_tc(const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p,

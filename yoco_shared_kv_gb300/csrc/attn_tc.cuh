@@ -14,17 +14,24 @@
 // owns pages [P c / C, P (c+1) / C) and each of its NW warps owns an equal
 // contiguous slice of that, streamed through the warp's own TMA ring. Every
 // worker therefore moves the same number of bytes, whatever the length mix,
-// and the ring never drains between segments.
+// and the ring never drains between segments. Where each warp's slice starts
+// is worked out once per step (attn_tc_plan) and read by every layer.
 //   - A segment that lies inside one warp's slice is finished in registers
 //     and written straight to `out`.
 //   - A segment cut by a warp boundary leaves a partial (m, l, o) per piece;
 //     at the end of the kernel the CTA combines the pieces of each segment
 //     it holds, writing `out` when the CTA holds the whole segment and a
 //     CTA-level partial otherwise.
-//   - A segment cut by a CTA boundary is finished by attn_tc_merge, which
-//     combines the CTA partials in CTA order.
+//   - A segment cut by a CTA boundary is finished inside the same launch:
+//     its CTAs meet at a counter, then each combines an equal share of the
+//     segment's outputs from all their partials, in CTA order.
 // Every combine runs in a fixed order that depends only on logical page
 // indices, so the output is bit-identical under any physical page placement.
+//
+// Code that runs once per launch (the prologue and everything after the
+// stream) is kept in rolled loops: it executes with a cold instruction
+// cache, where each straight-line block costs instruction fetches from L2 or
+// DRAM, so its size, more than its arithmetic, sets its time.
 //
 // Per page (one kv head, block_size tokens): K and V arrive by TMA as
 // head_dim/64 tiles of [block_size x 128 B] with the 128-byte swizzle (so
@@ -230,8 +237,8 @@ __device__ __forceinline__ int32_t owner(int64_t x, int64_t P, int32_t workers) 
     return static_cast<int32_t>(((x + 1) * workers - 1) / P);
 }
 
-// Most CTAs one merge can span (the grid has one CTA per SM).
-constexpr int kMaxMergePieces = 1024;
+// Most CTAs the grid may have (it has one CTA per SM).
+constexpr int kMaxCtas = 1024;
 
 struct PieceHdr {
     int64_t s0, s1;    // segment [first page, end) in the flattened order
@@ -241,40 +248,410 @@ struct PieceHdr {
     int32_t valid;
 };
 
+// ------------------------------------------------------------ per-step plan
+//
+// Where each warp's walk starts depends only on the step's metadata
+// (cross_query_start_loc, seq_lens, block_table) and the launch shape, and
+// every cross-decoder layer of a step walks the same cache with the same
+// metadata. attn_tc_plan works it out once per step; each layer's launch then
+// reads one 64-byte record per warp (its starting cursor and the block-table
+// entries of its first pages) instead of scanning the metadata, so its first
+// page copies leave after one dependent load.
+
+constexpr int kPlanBlk = 6;  // block-table entries of a walk's first pages kept in the plan
+constexpr uint32_t kPlanMagic = 0x594f434fu;
+
+struct __align__(16) WarpPlan {
+    int64_t P;          // pages of the launch
+    int64_t seg_start;  // cursor of the walk's first page (see Cursor)
+    int32_t req, n, g, pp, kv_len, pages;
+    int32_t blk[kPlanBlk];  // block-table entries of the walk's first pages
+};
+static_assert(sizeof(WarpPlan) == 64, "one plan record is four 16-byte loads");
+
+// The shapes a plan was made for: a launch checks them before it trusts the plan.
+struct __align__(16) PlanHdr {
+    uint32_t magic;
+    int32_t num_reqs, max_rows, H_kv, G, block_size, max_blocks, nw, ctas, stages, d;
+    int32_t pad[5];
+};
+static_assert(sizeof(PlanHdr) == 64, "plan header size");
+
 // The segments holding a CTA's first and last page, as seen by that CTA
-// (read by the merge kernel, so it needs no scan of the metadata itself).
-struct CtaHdr {
+// (read at the end of the launch by the cross-CTA merge).
+struct __align__(16) CtaHdr {
     int64_t P;       // pages of the launch
     int64_t a0, a1;  // segment of the first page [first, end); a0 < 0: slice starts past the end
     int64_t b0, b1;  // segment of the last page; b0 < 0: empty slice
     int32_t an, ag;  // (row, kv head) of segment a
     int32_t bn, bg;  // (row, kv head) of segment b
 };
+static_assert(sizeof(CtaHdr) == 64, "CTA header size");
 
-// Workspace carve-up: [W + C][2][G][D] partial outputs (warp pieces, then CTA
-// pieces), [W + C][2][G] (m, l), then one header per CTA.
+// Workspace carve-up (every part a multiple of 16 bytes):
+//   plan header, forward and reverse WarpPlan records [2][C][NW], CtaHdr [C],
+//   arrival counters [C] (one per CTA, used by the segment starting in it),
+//   [W + C][2][G][D] partial outputs (warp pieces, then CTA pieces),
+//   [W + C][2][G] (m, l).
 struct TcWs {
+    PlanHdr* plan;
+    WarpPlan* wplan;  // [2][C * NW]: forward walks, then reverse walks
+    CtaHdr* hdr;
+    uint32_t* cnt;
     float* w_o;
     float* c_o;
     float2* w_ml;
     float2* c_ml;
-    CtaHdr* hdr;
 };
 
 __host__ __device__ __forceinline__ int64_t tc_pieces(int64_t ctas, int nw, int G) {
     return (ctas * nw + ctas) * 2 * G;
 }
 
+__host__ __device__ __forceinline__ int64_t tc_plan_bytes(int64_t ctas, int nw) {
+    return static_cast<int64_t>(sizeof(PlanHdr)) + 2 * ctas * nw * sizeof(WarpPlan) +
+           ctas * sizeof(CtaHdr) + ((ctas * 4 + 15) & ~15ll);
+}
+
+// p.ws_o is the start of the workspace (16-byte aligned).
 __device__ __forceinline__ TcWs tc_ws(const AttnParams& p, int ctas, int nw, int D) {
     TcWs w;
+    uint8_t* base = reinterpret_cast<uint8_t*>(p.ws_o);
+    w.plan = reinterpret_cast<PlanHdr*>(base);
+    w.wplan = reinterpret_cast<WarpPlan*>(base + sizeof(PlanHdr));
+    w.hdr = reinterpret_cast<CtaHdr*>(w.wplan + 2ll * ctas * nw);
+    w.cnt = reinterpret_cast<uint32_t*>(w.hdr + ctas);
+    float* o = reinterpret_cast<float*>(base + tc_plan_bytes(ctas, nw));
     const int64_t per = 2ll * p.G;  // pieces per worker (first / last segment) x heads
     const int64_t W = static_cast<int64_t>(ctas) * nw;
-    w.w_o = p.ws_o;
-    w.c_o = p.ws_o + W * per * D;
-    w.w_ml = p.ws_ml;
-    w.c_ml = p.ws_ml + W * per;
-    w.hdr = reinterpret_cast<CtaHdr*>(p.ws_ml + tc_pieces(ctas, nw, p.G));
+    w.w_o = o;
+    w.c_o = o + W * per * D;
+    w.w_ml = reinterpret_cast<float2*>(o + tc_pieces(ctas, nw, p.G) * D);
+    w.c_ml = w.w_ml + W * per;
     return w;
+}
+
+__device__ __forceinline__ bool plan_matches(const PlanHdr& h, const AttnParams& p, int D,
+                                             int BS, int nw, int stages, int ctas) {
+    return h.magic == kPlanMagic && h.num_reqs == p.num_reqs && h.max_rows == p.max_rows &&
+           h.H_kv == p.H_kv && h.G == p.G && h.block_size == BS && h.max_blocks == p.max_blocks &&
+           h.nw == nw && h.ctas == ctas && h.stages == stages && h.d == D;
+}
+
+// Cursor of the first page of a walk over flattened pages [lo, hi) (forward:
+// lo, reverse: hi - 1), with the block-table entries of its first pages.
+// Warp-collective; lane 0 writes the record.
+__device__ void plan_walk(const AttnParams& p, int lane, int64_t P, int64_t lo, int64_t hi,
+                          bool rev, int32_t cap, WarpPlan* out) {
+    Cursor c;
+    c.req = -1;
+    c.seg_start = 0;
+    c.n = c.g = c.pp = c.kv_len = c.pages = 0;
+    int32_t blk[kPlanBlk];
+#pragma unroll
+    for (int i = 0; i < kPlanBlk; ++i) blk[i] = -1;
+    const int64_t n_my = hi - lo;
+    if (n_my > 0) {
+        locate(p, lane, rev ? hi - 1 : lo, cap, c);
+        if (c.req >= 0) {
+            Cursor w = c;
+#pragma unroll
+            for (int i = 0; i < kPlanBlk; ++i) {
+                if (i >= n_my) break;
+                blk[i] = __ldg(p.block_table + static_cast<int64_t>(w.req) * p.max_blocks + w.pp);
+                if (rev) retreat(p, w, cap);
+                else advance(p, w, cap);
+            }
+        }
+    }
+    if (lane == 0) {
+        out->P = P;
+        out->seg_start = c.seg_start;
+        out->req = c.req;
+        out->n = c.n;
+        out->g = c.g;
+        out->pp = c.pp;
+        out->kv_len = c.kv_len;
+        out->pages = c.pages;
+#pragma unroll
+        for (int i = 0; i < kPlanBlk; ++i) out->blk[i] = blk[i];
+    }
+}
+
+// The per-step plan: one CTA per attention CTA, one warp per attention warp.
+// Reads the metadata, then (after the dependency wait, since the previous
+// kernel may be a layer still using the workspace) writes the records, the
+// CTA headers and zeroes the arrival counters.
+template <int NW, int STAGES, int D, int BS>
+__global__ void __launch_bounds__(NW * 32) attn_tc_plan(const AttnParams p) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const TcWs ws = tc_ws(p, gridDim.x, NW, D);
+    const int64_t cap64 = static_cast<int64_t>(p.max_blocks) * BS;
+    const int32_t cap = cap64 > 0x7fffffff ? 0x7fffffff : static_cast<int32_t>(cap64);
+    const int64_t P = total_pages(p, lane, cap);
+    const int64_t C = gridDim.x;
+    const int64_t cta_lo = P * blockIdx.x / C, cta_hi = P * (blockIdx.x + 1) / C;
+    const int64_t my_lo = cta_lo + (cta_hi - cta_lo) * warp / NW;
+    const int64_t my_hi = cta_lo + (cta_hi - cta_lo) * (warp + 1) / NW;
+    // header fields: warp 0 the segment of page cta_lo, warp 1 that of page cta_hi - 1
+    int64_t hs0 = -1, hs1 = -1;
+    int32_t hn = 0, hg = 0;
+    if (warp <= 1) {
+        const int64_t x = warp == 0 ? cta_lo : cta_hi - 1;
+        const bool any = warp == 0 ? cta_lo < P : cta_hi > cta_lo;
+        if (any) {
+            Cursor h;
+            locate(p, lane, x, cap, h);
+            if (h.req >= 0) {
+                hs0 = h.seg_start;
+                hs1 = h.seg_start + h.pages;
+                hn = h.n;
+                hg = h.g;
+            }
+        }
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int64_t wid = static_cast<int64_t>(blockIdx.x) * NW + warp;
+    plan_walk(p, lane, P, my_lo, my_hi, false, cap, ws.wplan + wid);
+    plan_walk(p, lane, P, my_lo, my_hi, true, cap, ws.wplan + C * NW + wid);
+    if (lane == 0 && warp <= 1) {
+        CtaHdr* hp = ws.hdr + blockIdx.x;
+        if (warp == 0) {
+            hp->P = P;
+            hp->a0 = hs0;
+            hp->a1 = hs1;
+            hp->an = hn;
+            hp->ag = hg;
+        } else {
+            hp->b0 = hs0;
+            hp->b1 = hs1;
+            hp->bn = hn;
+            hp->bg = hg;
+        }
+    }
+    if (threadIdx.x == 0) {
+        ws.cnt[blockIdx.x] = 0u;
+        if (blockIdx.x == 0) {
+            PlanHdr h = {};
+            h.magic = kPlanMagic;
+            h.num_reqs = p.num_reqs;
+            h.max_rows = p.max_rows;
+            h.H_kv = p.H_kv;
+            h.G = p.G;
+            h.block_size = BS;
+            h.max_blocks = p.max_blocks;
+            h.nw = NW;
+            h.ctas = static_cast<int32_t>(C);
+            h.stages = STAGES;
+            h.d = D;
+            *ws.plan = h;
+        }
+    }
+}
+
+// ------------------------------------------------------- cross-CTA arrival
+//
+// The CTAs that share a segment cut by CTA boundaries meet at a counter kept
+// by the segment's first CTA: that CTA adds 2^31 - (n - 1), the n - 1 others
+// add 1, so the counter's top bit flips exactly when the last of them
+// arrives, and its low 31 bits are back to zero for the next launch (the
+// plan zeroes the counters once). A CTA has arrived at all of its (at most
+// two) counters before it waits on any, so the waits cannot form a cycle;
+// every CTA of the grid is resident (one per SM), and each wait is bounded.
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Spin until the top bit of *cnt differs from that of `old`; false on give-up.
+__device__ __forceinline__ bool wait_flip(const uint32_t* cnt, uint32_t old, uint64_t limit_ns) {
+    if ((ld_acquire_u32(cnt) ^ old) & 0x80000000u) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1; it < (1u << 26); ++it) {
+        if ((ld_acquire_u32(cnt) ^ old) & 0x80000000u) return true;
+        if ((it & 15u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
+    }
+    return false;
+}
+
+// Finishes the segments cut by CTA boundaries, inside the split kernel.
+//
+// Each CTA holding pages of such a segment (a holder) has written its
+// CTA-level partial (m, l, o) to the workspace; it arrives at the segment's
+// counter and, once every holder has arrived, takes an equal share of the
+// segment's G x D outputs and combines all holders' partials for it in holder
+// order (so the result depends only on logical page positions). A CTA holds
+// at most two such segments (those of its first and last page); with two, the
+// two halves of the CTA work on them at the same time.
+//
+// The share is finished with one round of global loads: every (holder,
+// output) value and every (holder, head) statistic of the share is loaded at
+// once into `scratch` (the CTA's ring, idle by now), then the factors and
+// sums are formed in shared memory in a fixed order.
+__device__ __forceinline__ uint32_t atom_add_release_u32(uint32_t* p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.add.release.gpu.global.u32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(p), "r"(v)
+                 : "memory");
+    return old;
+}
+
+// Largest scratch (floats, a multiple of 4) one segment's share needs with H
+// holders: the share's outputs of every holder (shares are whole 16-byte
+// vectors: at most G*D + 4H), 3 floats per (holder, head) it touches (at most
+// 2 heads once H >= G, else at most G/H + 3) and one per head.
+__host__ __device__ __forceinline__ int merge_scratch_floats(int ctas, int G, int D) {
+    return (G * D + 10 * ctas + 14 * (G + 1) + 4 + 3) & ~3;
+}
+
+template <int D>
+__device__ __forceinline__ void cross_cta_merge(const AttnParams& p, const TcWs& ws,
+                                                const CtaHdr& Hc, float* scratch) {
+    const int32_t c = blockIdx.x, ctas = gridDim.x;
+    const int nthr = static_cast<int>(blockDim.x);
+    const int64_t P = Hc.P;
+    if (P <= 0) return;
+    const int G = p.G;
+    if (!(P * c / ctas < P * (c + 1) / ctas)) return;  // a CTA without pages holds no partial
+
+    // The (at most two) cut segments: {first page, row, kv head, first CTA,
+    // holders, this CTA's rank among them}. Holders are the CTAs of the span
+    // with pages: all of them when P >= ctas; otherwise each holder has
+    // exactly one page of the segment and holder j owns page s0 + j.
+    struct Seg {
+        int64_t s0;
+        int32_t n, g, cf, nsh, rank;
+    };
+    Seg sg0 = {}, sg1 = {};
+    int nseg = 0;
+    const bool dense = P >= ctas;
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+        const int64_t s0 = which == 0 ? Hc.a0 : Hc.b0, s1 = which == 0 ? Hc.a1 : Hc.b1;
+        if (s0 < 0 || (which == 1 && s0 == Hc.a0)) continue;
+        const int32_t c_first = owner(s0, P, ctas), c_last = owner(s1 - 1, P, ctas);
+        // not cut (finished above), or this CTA holds none of it
+        if (c_first == c_last || c < c_first || c > c_last) continue;
+        Seg x;
+        x.s0 = s0;
+        x.n = which == 0 ? Hc.an : Hc.bn;
+        x.g = which == 0 ? Hc.ag : Hc.bg;
+        x.cf = c_first;
+        x.nsh = dense ? c_last - c_first + 1 : static_cast<int32_t>(s1 - s0);
+        x.rank = dense ? c - c_first : static_cast<int32_t>(P * c / ctas - s0);
+        if (nseg == 0) sg0 = x;
+        else sg1 = x;
+        ++nseg;
+    }
+    if (nseg == 0) return;
+
+    // arrive at every counter (release: this CTA's partials, written before
+    // the barrier above, are published with it), then wait on each (acquire)
+    int* ok_flag = reinterpret_cast<int*>(scratch);
+    if (threadIdx.x == 0) {
+        const uint32_t old0 =
+            atom_add_release_u32(ws.cnt + sg0.cf, c == sg0.cf ? 0x80000000u - (sg0.nsh - 1) : 1u);
+        const uint32_t old1 =
+            nseg == 2 ? atom_add_release_u32(ws.cnt + sg1.cf,
+                                             c == sg1.cf ? 0x80000000u - (sg1.nsh - 1) : 1u)
+                      : 0u;
+        bool ok = wait_flip(ws.cnt + sg0.cf, old0, kWaitLimitNs);
+        if (ok && nseg == 2) ok = wait_flip(ws.cnt + sg1.cf, old1, kWaitLimitNs);
+        if (!ok) set_err(p.err, YOCO_DEVERR_TIMEOUT);
+        *ok_flag = ok ? 1 : 0;
+    }
+    __syncthreads();
+    if (!*ok_flag) return;
+
+    const int half = nseg == 2 ? nthr / 2 : nthr;
+    const int si = nseg == 2 ? static_cast<int>(threadIdx.x) / half : 0;
+    const int tl = static_cast<int>(threadIdx.x) - si * half;  // thread index within the half
+    const Seg sg = si == 0 ? sg0 : sg1;
+    const int nh_ = sg.nsh;
+    // this CTA's share of the segment's G x D outputs (whole 16-byte vectors),
+    // and the heads it touches
+    const int total = G * D;
+    const int per = ((total + nh_ - 1) / nh_ + 3) & ~3;
+    const int lo = min(total, sg.rank * per), hi = min(total, lo + per);
+    const int nout = hi - lo, nv = nout >> 2;
+    const int h_lo = lo / D, nhd = nout > 0 ? (hi - 1) / D - h_lo + 1 : 0;
+    float* so = scratch + 16 + si * merge_scratch_floats(ctas, G, D);  // [holder][nout]
+    float2* sml = reinterpret_cast<float2*>(so + nh_ * nout);          // [holder][nhd]
+    float* sf = reinterpret_cast<float*>(sml + nh_ * nhd);             // [holder][nhd] 2^(m - M)
+    float* sInvL = sf + nh_ * nhd;                                     // [nhd]
+    // holder j's partial slot: the segment begins in holder 0's slice (slot 1);
+    // for every other holder it is the first segment (slot 0)
+    auto slot = [&](int j) -> int64_t {
+        const int64_t cj = dense ? sg.cf + j : owner(sg.s0 + j, P, ctas);
+        return (cj * 2 + (j == 0 ? 1 : 0)) * G;
+    };
+    // One round of asynchronous global -> shared copies: every holder's
+    // outputs of the share (16-byte vectors) and (m, l) of its heads. The
+    // loops stay rolled: this code runs once per launch, where instruction
+    // fetch, not the copies, sets the time.
+#pragma unroll 1
+    for (int j = tl; j < nh_ * nv; j += half) {
+        const int hj = j / nv, v = j - hj * nv;
+        cp_async_16(so + hj * nout + 4 * v, ws.c_o + slot(hj) * D + lo + 4 * v);
+    }
+#pragma unroll 1
+    for (int k = tl; k < nh_ * nhd; k += half) {
+        const int hj = k / nhd;
+        cp_async_8(sml + k, ws.c_ml + slot(hj) + h_lo + (k - hj * nhd));
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    // factors: for each head of the share, M = max over holders, f_j = 2^(m_j - M),
+    // L = sum l_j f_j. One warp per head, lanes over holders; the reductions
+    // are fixed butterfly trees, so the result does not depend on timing.
+    const int nwh = half >> 5, wl = tl >> 5, ln = tl & 31;
+#pragma unroll 1
+    for (int hh = wl; hh < nhd; hh += nwh) {
+        float M = -INFINITY;
+#pragma unroll 1
+        for (int j = ln; j < nh_; j += 32) M = fmaxf(M, sml[j * nhd + hh].x);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        float L = 0.f;
+#pragma unroll 1
+        for (int j = ln; j < nh_; j += 32) {
+            const float2 ml = sml[j * nhd + hh];
+            const float f = ml.x != -INFINITY ? exp2_approx(ml.x - M) : 0.f;
+            sf[j * nhd + hh] = f;
+            L += ml.y * f;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+        if (ln == 0) sInvL[hh] = 1.f / L;
+    }
+    __syncthreads();
+    __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out);
+    const int64_t head0 = static_cast<int64_t>(sg.n) * p.H_q + sg.g * G;
+    // a holder with no key has f = 0 and a slot never written: select, not 0 * x
+    auto term = [&](int j, int e, int hh) {
+        const float f = sf[j * nhd + hh];
+        return f != 0.f ? so[j * nout + e] * f : 0.f;
+    };
+#pragma unroll 1
+    for (int e = tl; e < nout; e += half) {
+        const int hh = (lo + e) / D - h_lo;
+        // four independent chains over the holders (j mod 4), summed in a fixed order
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        int j = 0;
+#pragma unroll 1
+        for (; j + 4 <= nh_; j += 4) {
+            a0 += term(j, e, hh);
+            a1 += term(j + 1, e, hh);
+            a2 += term(j + 2, e, hh);
+            a3 += term(j + 3, e, hh);
+        }
+#pragma unroll 1
+        for (; j < nh_; ++j) a0 += term(j, e, hh);
+        outp[head0 * D + lo + e] = __float2bfloat16_rn(((a0 + a1) + (a2 + a3)) * sInvL[hh]);
+    }
 }
 
 // --------------------------------------------------------------- kernel
@@ -297,37 +674,74 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
     __shared__ __align__(16) float4 stage_scale[F8 ? NW * STAGES : 1];
     __shared__ PieceHdr hdr[NW][2];
     __shared__ int abort_flag;
+    __shared__ __align__(16) CtaHdr cta_hdr;  // this CTA's first / last segment (from the plan)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gl = lane >> 2, tq = lane & 3;  // mma fragment row group / column pair
-    if (threadIdx.x == 0) abort_flag = launch_aborted(p) ? 1 : 0;
-    if (lane == 0) {
-        for (int i = 0; i < STAGES; ++i) mbar_init(&bars[warp * STAGES + i], 1);
+    const TcWs ws = tc_ws(p, gridDim.x, NW, D);
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    uint8_t* wbuf = smem + warp * STAGES * S::STAGE_BYTES;
+    uint64_t* wbar = bars + warp * STAGES;
+    if (lane == 0) {  // each warp's own ring barriers: only this warp waits on them
+        for (int i = 0; i < STAGES; ++i) mbar_init(&wbar[i], 1);
         fence_mbar_init();
         hdr[warp][0].valid = hdr[warp][1].valid = 0;
     }
+    __syncwarp();
+    // This warp's plan record (the forward or the reverse walk): four
+    // independent loads, the only dependent step before the first page copies.
+    static_assert(STAGES <= kPlanBlk, "the plan holds the block ids of the prologue's pages");
+    uint4 r0, r1, r2, r3;
+    {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            ws.wplan + (REV ? static_cast<int64_t>(gridDim.x) * NW : 0) +
+            static_cast<int64_t>(blockIdx.x) * NW + warp);
+        r0 = __ldg(src);
+        r1 = __ldg(src + 1);
+        r2 = __ldg(src + 2);
+        r3 = __ldg(src + 3);
+    }
+    int plan_state = 0;  // thread 0: 0 plan usable, 1 launch already aborted, 2 no matching plan
     if (threadIdx.x == 0) {
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
+        const uint4* hs = reinterpret_cast<const uint4*>(ws.plan);
+        const uint4* cs = reinterpret_cast<const uint4*>(ws.hdr + blockIdx.x);
+        uint4 h[4], c[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            h[i] = __ldg(hs + i);
+            c[i] = __ldg(cs + i);
+        }
+        PlanHdr ph;
+        ph.magic = h[0].x;
+        ph.num_reqs = static_cast<int32_t>(h[0].y);
+        ph.max_rows = static_cast<int32_t>(h[0].z);
+        ph.H_kv = static_cast<int32_t>(h[0].w);
+        ph.G = static_cast<int32_t>(h[1].x);
+        ph.block_size = static_cast<int32_t>(h[1].y);
+        ph.max_blocks = static_cast<int32_t>(h[1].z);
+        ph.nw = static_cast<int32_t>(h[1].w);
+        ph.ctas = static_cast<int32_t>(h[2].x);
+        ph.stages = static_cast<int32_t>(h[2].y);
+        ph.d = static_cast<int32_t>(h[2].z);
+        uint4* cd = reinterpret_cast<uint4*>(&cta_hdr);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) cd[i] = c[i];
+        plan_state = launch_aborted(p) ? 1
+                     : plan_matches(ph, p, D, BS, NW, STAGES, static_cast<int>(gridDim.x)) ? 0 : 2;
     }
-    __syncthreads();
-    if (abort_flag) return;
-
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                               ~static_cast<uintptr_t>(1023));
-    const int64_t cap64 = static_cast<int64_t>(p.max_blocks) * BS;
-    const int32_t cap = cap64 > 0x7fffffff ? 0x7fffffff : static_cast<int32_t>(cap64);
-    const int64_t P = total_pages(p, lane, cap);
+    const int64_t P = static_cast<int64_t>((static_cast<uint64_t>(r0.y) << 32) | r0.x);
     const int64_t C = gridDim.x;
     const int64_t cta_lo = P * blockIdx.x / C, cta_hi = P * (blockIdx.x + 1) / C;
     const int64_t my_lo = cta_lo + (cta_hi - cta_lo) * warp / NW;
     const int64_t my_hi = cta_lo + (cta_hi - cta_lo) * (warp + 1) / NW;
-    const int32_t n_my = static_cast<int32_t>(my_hi - my_lo);
+    int32_t n_my = static_cast<int32_t>(my_hi - my_lo);
     const int32_t wid = blockIdx.x * NW + warp;
-    const TcWs ws = tc_ws(p, gridDim.x, NW, D);
+    const int64_t cap64 = static_cast<int64_t>(p.max_blocks) * BS;
+    const int32_t cap = cap64 > 0x7fffffff ? 0x7fffffff : static_cast<int32_t>(cap64);
 
-    uint8_t* wbuf = smem + warp * STAGES * S::STAGE_BYTES;
-    uint64_t* wbar = bars + warp * STAGES;
     // Odd layers may walk each slice backwards (REV): a layer then starts on
     // the pages the previous layer read last, which are still in L2.
     constexpr bool rev = REV;
@@ -336,24 +750,23 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
         else advance(p, c, cap);
     };
     Cursor cc;  // page being consumed
-    cc.req = -1;
-    if (n_my > 0) locate(p, lane, rev ? my_hi - 1 : my_lo, cap, cc);
-    // header for the merge kernel: warp 0 finds the segment of page cta_lo,
-    // warp 1 the segment of page cta_hi - 1
-    int64_t hs0 = -1, hs1 = -1;
-    int32_t hn = 0, hg = 0;
-    if (warp <= 1) {
-        const int64_t x = warp == 0 ? cta_lo : cta_hi - 1;
-        const bool any = warp == 0 ? cta_lo < P : cta_hi > cta_lo;
-        Cursor h0 = cc;
-        if (any && !(warp == 0 && n_my > 0 && !rev)) locate(p, lane, x, cap, h0);
-        if (any && h0.req >= 0) {
-            hs0 = h0.seg_start;
-            hs1 = h0.seg_start + h0.pages;
-            hn = h0.n;
-            hg = h0.g;
-        }
-    }
+    cc.seg_start = static_cast<int64_t>((static_cast<uint64_t>(r0.w) << 32) | r0.z);
+    cc.req = static_cast<int32_t>(r1.x);
+    cc.n = static_cast<int32_t>(r1.y);
+    cc.g = static_cast<int32_t>(r1.z);
+    cc.pp = static_cast<int32_t>(r1.w);
+    cc.kv_len = static_cast<int32_t>(r2.x);
+    cc.pages = static_cast<int32_t>(r2.y);
+    const int32_t plan_blk[kPlanBlk] = {static_cast<int32_t>(r2.z), static_cast<int32_t>(r2.w),
+                                        static_cast<int32_t>(r3.x), static_cast<int32_t>(r3.y),
+                                        static_cast<int32_t>(r3.z), static_cast<int32_t>(r3.w)};
+    // A record that does not describe a page of this launch (a plan for other
+    // metadata, or none) must not steer a copy: nothing is issued, and the
+    // header check below ends the launch.
+    const bool rec_ok = P >= 0 && cc.req >= 0 && cc.req < p.num_reqs && cc.g >= 0 &&
+                        cc.g < p.H_kv && cc.n >= 0 && cc.n < p.max_rows && cc.pages > 0 &&
+                        cc.pp >= 0 && cc.pp < cc.pages && static_cast<int64_t>(cc.pages) * BS <= cap64 + BS;
+    if (!rec_ok || n_my < 0) n_my = 0;
     Cursor pc = cc;  // next page to issue (lane 0)
     // lane 0: block-table entry of page pc, loaded one issue ahead so that its
     // latency overlaps the page computed in between
@@ -405,12 +818,27 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
                           p.scales + static_cast<int64_t>(blk) * p.H_kv + pc.g, 16, bar);
         }
         step(pc);
-        if (i + 1 < n_my) fetch_blk();
     };
+    const int pro = n_my < STAGES ? n_my : STAGES;
     if (lane == 0) {
-        if (n_my > 0) fetch_blk();
-        const int pro = n_my < STAGES ? n_my : STAGES;
-        for (int i = 0; i < pro; ++i) issue(i);
+        // the prologue's pages take their block ids from the plan
+#pragma unroll
+        for (int i = 0; i < STAGES; ++i) {
+            if (i < pro) {
+                blk_next = plan_blk[i];
+                issue(i);
+            }
+        }
+        if (pro < n_my) fetch_blk();
+    }
+    if (threadIdx.x == 0) abort_flag = plan_state;
+    __syncthreads();  // every ring's barriers initialised; the plan checked
+    if (abort_flag) {
+        // a launch that has already failed, or a workspace without a plan for
+        // these shapes: drain the copies issued above, flag, and end
+        for (int i = 0; i < pro; ++i) (void)mbar_wait_bounded(wbar + i, 0, kWaitLimitNs);
+        if (threadIdx.x == 0 && abort_flag == 2) set_err(p.err, YOCO_DEVERR_PLAN);
+        return;
     }
     // When launched as a programmatic dependent of the previous kernel in the
     // stream (the caller allows it only when that kernel writes neither), the
@@ -482,22 +910,6 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
             }
         }
     }
-    if (lane == 0 && warp <= 1) {
-        CtaHdr* hp = ws.hdr + blockIdx.x;
-        if (warp == 0) {
-            hp->P = P;
-            hp->a0 = hs0;
-            hp->a1 = hs1;
-            hp->an = hn;
-            hp->ag = hg;
-        } else {
-            hp->b0 = hs0;
-            hp->b1 = hs1;
-            hp->bn = hn;
-            hp->bg = hg;
-        }
-    }
-
     uint32_t qf[S::KD][NT][2];
     float o[S::KD][NT][4];
     float m_run[NT][2], l_part[NT][2];
@@ -859,7 +1271,10 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
             }
         }
         __syncwarp();
-        if (lane == 0 && i + STAGES < n_my) issue(i + STAGES);
+        if (lane == 0 && i + STAGES < n_my) {
+            issue(i + STAGES);
+            if (i + STAGES + 1 < n_my) fetch_blk();
+        }
 
         if (cc.pp == (rev ? 0 : cc.pages - 1) || i == n_my - 1) {  // segment or slice done
 #pragma unroll
@@ -1064,156 +1479,12 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
         }
         e0 = e1;
     }
-    // the merge kernel may be scheduled now (it waits for this grid to finish);
-    // triggering only here keeps its waiting CTAs off the SM during the combine
+    __syncthreads();  // every CTA-level partial of this CTA has been written
+    // The next kernel in the stream (the next layer) may be scheduled now: it
+    // can only take an SM as this grid's CTAs exit, and it waits for the whole
+    // grid before it touches the workspace, queries or outputs.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-// Finishes every segment cut by a CTA boundary from the CTA-level partials
-// (rows with no key are zero-filled by the split kernel). Grid: one CTA per
-// split-kernel CTA.
-// Each CTA spanned by a cut segment takes an equal share of that segment's
-// G x D outputs, so a long segment's merge spreads over all of its CTAs. A
-// CTA shares at most two segments (those of its first and last page); the
-// two halves of the CTA work on them at the same time. Pieces are combined
-// in CTA order.
-constexpr int kMergeThreads = 256;
-constexpr int kMergeHalf = kMergeThreads / 2;
-constexpr int kMergeRegPieces = 8;  // per-thread piece statistics kept in registers
-
-template <int D, int NW>
-__global__ void __launch_bounds__(kMergeThreads) attn_tc_merge(const AttnParams p, int32_t ctas) {
-    extern __shared__ float fac[];  // [2][pieces][G]: 2^(m - M) per CTA piece and head
-    __shared__ float red[kMergeThreads];
-    __shared__ float headM[2][16], headInvL[2][16];
-    const int32_t c = blockIdx.x;
-    __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out);
-    // launched as a programmatic dependent of attn_tc_persistent: wait for it,
-    // and let the next kernel (the next layer's split) start its prologue
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const TcWs ws = tc_ws(p, ctas, NW, D);
-    const CtaHdr Hc = ws.hdr[c];
-
-    if (launch_aborted(p)) return;
-    const int64_t P = Hc.P;
-    if (P <= 0) return;
-    const int G = p.G;
-
-    // the (at most two) cut segments this CTA shares
-    int64_t seg0[2];
-    int32_t segn[2], segg[2], cf[2], np_[2];
-    int nseg = 0;
-    for (int which = 0; which < 2; ++which) {
-        const int64_t s0 = which == 0 ? Hc.a0 : Hc.b0, s1 = which == 0 ? Hc.a1 : Hc.b1;
-        if (s0 < 0 || (which == 1 && s0 == Hc.a0)) continue;
-        const int32_t c_first = owner(s0, P, ctas), c_last = owner(s1 - 1, P, ctas);
-        // not cut (finished in the split kernel), or this CTA holds none of it
-        // (an empty CTA right before c_first starts at the segment's first page)
-        if (c_first == c_last || c < c_first || c > c_last) continue;
-        seg0[nseg] = s0;
-        segn[nseg] = which == 0 ? Hc.an : Hc.bn;
-        segg[nseg] = which == 0 ? Hc.ag : Hc.bg;
-        cf[nseg] = c_first;
-        np_[nseg] = c_last - c_first + 1;
-        ++nseg;
-    }
-    if (nseg == 0) return;
-    (void)seg0;
-    // threads [0, half) take segment 0, [half, 2 half) segment 1 (all of them
-    // take segment 0 when there is only one)
-    const int half = nseg == 2 ? kMergeHalf : kMergeThreads;
-    const int si = nseg == 2 ? static_cast<int>(threadIdx.x) / kMergeHalf : 0;
-    const int tl = static_cast<int>(threadIdx.x) - si * half;  // thread index within the half
-    const int32_t c_first = cf[si], np = np_[si];
-    const int k = c - c_first;  // this CTA's share of the outputs
-    auto nonempty = [&](int32_t cc_) { return P * cc_ / ctas < P * (cc_ + 1) / ctas; };
-    // CTA c_first keeps slot 1 (the segment begins in its slice); the others slot 0
-    auto piece = [&](int i) -> int64_t {
-        return (static_cast<int64_t>(c_first + i) * 2 + (i == 0 ? 1 : 0)) * G;
-    };
-    float* ftab = fac + si * ctas * G;
-    // per-head max and sum over the pieces: thread tl handles head tl % 16
-    const int h16 = tl & 15, sub = tl >> 4, nsub = half >> 4;
-    float2 mlr[kMergeRegPieces];
-    float mloc = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < kMergeRegPieces; ++j) {
-        const int i = sub + j * nsub;
-        mlr[j] = make_float2(-INFINITY, 0.f);
-        if (h16 < G && i < np && nonempty(c_first + i)) mlr[j] = ws.c_ml[piece(i) + h16];
-        mloc = fmaxf(mloc, mlr[j].x);
-    }
-    for (int i = sub + kMergeRegPieces * nsub; h16 < G && i < np; i += nsub)  // rare: long spans
-        if (nonempty(c_first + i)) mloc = fmaxf(mloc, ws.c_ml[piece(i) + h16].x);
-    red[threadIdx.x] = mloc;
-    __syncthreads();
-    if (tl < 16) {
-        float M = -INFINITY;
-        for (int j = 0; j < nsub; ++j) M = fmaxf(M, red[si * half + j * 16 + tl]);
-        headM[si][tl] = M;
-    }
-    __syncthreads();
-    float lloc = 0.f;
-    if (h16 < G) {
-        const float M = headM[si][h16];
-#pragma unroll
-        for (int j = 0; j < kMergeRegPieces; ++j) {
-            const int i = sub + j * nsub;
-            if (i < np) {
-                const float f = mlr[j].x != -INFINITY ? exp2_approx(mlr[j].x - M) : 0.f;
-                lloc += mlr[j].y * f;
-                ftab[i * G + h16] = f;
-            }
-        }
-        for (int i = sub + kMergeRegPieces * nsub; i < np; i += nsub) {
-            float f = 0.f;
-            if (nonempty(c_first + i)) {
-                const float2 ml = ws.c_ml[piece(i) + h16];
-                if (ml.x != -INFINITY) f = exp2_approx(ml.x - M);
-                lloc += ml.y * f;
-            }
-            ftab[i * G + h16] = f;
-        }
-    }
-    red[threadIdx.x] = lloc;
-    __syncthreads();
-    if (tl < 16) {
-        float L = 0.f;
-        for (int j = 0; j < nsub; ++j) L += red[si * half + j * 16 + tl];
-        headInvL[si][tl] = 1.f / L;
-    }
-    __syncthreads();
-    // this CTA's share of the segment's G x D outputs
-    const int total = G * D;
-    const int per = (total + np - 1) / np;
-    const int lo = k * per, hi = min(total, lo + per);
-    const int64_t head0 = static_cast<int64_t>(segn[si]) * p.H_q + segg[si] * G;
-    const int64_t st = static_cast<int64_t>(2) * G * D;
-    for (int idx = lo + tl; idx < hi; idx += half) {
-        const int h = idx / D;
-        // an empty CTA's slot was never written (stale, maybe NaN): select, never scale by 0
-        const float f0 = ftab[h];
-        const float v0 = ws.c_o[piece(0) * D + idx];  // slot 1 of c_first
-        float acc = f0 != 0.f ? v0 * f0 : 0.f;
-        const float* b1 = ws.c_o + (static_cast<int64_t>(c_first) * 2 * G) * D + idx;
-        int i = 1;
-        for (; i + 8 <= np; i += 8) {  // eight independent loads in flight
-            float a[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) a[u] = b1[st * (i + u)];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const float f = ftab[(i + u) * G + h];
-                acc += f != 0.f ? a[u] * f : 0.f;
-            }
-        }
-        for (; i < np; ++i) {
-            const float f = ftab[i * G + h];
-            acc += f != 0.f ? b1[st * i] * f : 0.f;
-        }
-        outp[head0 * D + idx] = __float2bfloat16_rn(acc * headInvL[si][h]);
-    }
+    cross_cta_merge<D>(p, ws, cta_hdr, reinterpret_cast<float*>(smem));
 }
 
 // One-time (per device) setting of a kernel's dynamic shared memory limit.
@@ -1236,47 +1507,43 @@ cudaError_t launch_one(const CUtensorMap& mk, const CUtensorMap& mv, const AttnP
                        cudaStream_t s) {
     using S = TcShape<D, BS, F8, NT>;
     static unsigned long long smem_fwd = 0, smem_rev = 0, smem_fuse = 0;  // one per kernel
-    const bool fuse = p.k_new != nullptr;
-    auto kernel = fuse ? attn_tc_persistent<D, BS, NT, false, F8, true>
-                       : (p.reverse ? attn_tc_persistent<D, BS, NT, true, F8, false>
-                                    : attn_tc_persistent<D, BS, NT, false, F8, false>);
-    cudaError_t e = ensure_smem_attr(kernel, S::SMEM,
-                                     fuse ? smem_fuse : (p.reverse ? smem_rev : smem_fwd));
-    if (e != cudaSuccess) return e;
     const int ctas = tc_ctas(sms);
-    AttnParams q = p;  // workspace: outputs of all pieces, then their (m, l), then headers
-    q.ws_ml = reinterpret_cast<float2*>(p.ws_o + tc_pieces(ctas, S::NW, p.G) * D);
-    // The merge grid is a programmatic dependent of the split grid: it is
-    // scheduled while the split grid drains and waits (griddepcontrol.wait)
-    // before reading its partials. The split grid is one of the kernel before
-    // it only when the caller allows the overlap: it then runs its metadata
-    // prologue and first page copies while that kernel (for example the
-    // previous layer's merge) drains, and waits before it touches queries,
-    // outputs or the workspace.
+    // the cross-CTA merge keeps its tables in the (then idle) ring
+    if ((16 + 2 * merge_scratch_floats(ctas, 16, D)) * 4 > S::SMEM - 1024)
+        return cudaErrorInvalidConfiguration;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ctas);
     cfg.blockDim = dim3(S::NW * 32);
-    cfg.dynamicSmemBytes = S::SMEM;
     cfg.stream = s;
     cfg.attrs = attr;
-    cfg.numAttrs = p.overlap ? 1 : 0;
-    e = cudaLaunchKernelEx(&cfg, kernel, mk, mv, q);
-    if (e != cudaSuccess) return e;
-    cfg.numAttrs = 1;
-    const int msmem = 2 * ctas * p.G * static_cast<int>(sizeof(float));  // factor tables
-    const int msmem_max = 2 * ctas * 16 * static_cast<int>(sizeof(float));  // largest group
-    if (msmem_max > 48 * 1024) {  // only ever raise the limit above the default
-        static unsigned long long merge_smem_set = 0;
-        e = ensure_smem_attr(attn_tc_merge<D, S::NW>, msmem_max, merge_smem_set);
-        if (e != cudaSuccess) return e;
+    cudaError_t e;
+    if (!p.planned) {
+        // The step's plan. It may start while the previous kernel drains when
+        // the caller allows the overlap (it reads only the metadata before its
+        // dependency wait); the attention launch below reads the plan at its
+        // very start, so it is an ordinary (fully ordered) launch.
+        cfg.dynamicSmemBytes = 0;
+        cfg.numAttrs = p.overlap ? 1 : 0;
+        e = cudaLaunchKernelEx(&cfg, attn_tc_plan<S::NW, S::STAGES, D, BS>, p);
+        if (e != cudaSuccess || p.plan_only) return e;
     }
-    cfg.gridDim = dim3(ctas);
-    cfg.blockDim = dim3(kMergeThreads);
-    cfg.dynamicSmemBytes = msmem;
-    return cudaLaunchKernelEx(&cfg, attn_tc_merge<D, S::NW>, q, static_cast<int32_t>(ctas));
+    const bool fuse = p.k_new != nullptr;
+    auto kernel = fuse ? attn_tc_persistent<D, BS, NT, false, F8, true>
+                       : (p.reverse ? attn_tc_persistent<D, BS, NT, true, F8, false>
+                                    : attn_tc_persistent<D, BS, NT, false, F8, false>);
+    e = ensure_smem_attr(kernel, S::SMEM, fuse ? smem_fuse : (p.reverse ? smem_rev : smem_fwd));
+    if (e != cudaSuccess) return e;
+    // With a plan made earlier and the caller's leave, the launch is a
+    // programmatic dependent of the kernel before it (for example the previous
+    // layer): its prologue (plan record, first page copies) overlaps that
+    // kernel's end, and it waits before touching queries, outputs or the
+    // workspace.
+    cfg.dynamicSmemBytes = S::SMEM;
+    cfg.numAttrs = (p.planned && p.overlap) ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, mk, mv, p);
 }
 
 template <int D, bool F8>

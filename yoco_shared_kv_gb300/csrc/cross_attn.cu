@@ -171,9 +171,11 @@ yoco_status_t run_attn(const void* q, const void* k_cache, const void* v_cache,
                        int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale,
                        yoco_dtype_t dtype, uint32_t flags, void* workspace,
                        size_t workspace_bytes, int32_t* err_word, void* stream,
-                       const void* k_new = nullptr, const void* v_new = nullptr) {
+                       const void* k_new = nullptr, const void* v_new = nullptr,
+                       bool plan_only = false) {
     const bool e4m3 = dtype == YOCO_E4M3;
-    if (flags & ~static_cast<uint32_t>(YOCO_ATTN_REVERSE | YOCO_ATTN_OVERLAP | YOCO_ATTN_KEEP_TAIL))
+    if (flags & ~static_cast<uint32_t>(YOCO_ATTN_REVERSE | YOCO_ATTN_OVERLAP |
+                                       YOCO_ATTN_KEEP_TAIL | YOCO_ATTN_PLANNED))
         return YOCO_ERR_INVALID_ARG;
     if (!(dtype_ok(dtype) || e4m3) || !head_dim_ok(head_dim) || !block_size_ok(block_size) ||
         (e4m3 && head_dim == 64))
@@ -185,12 +187,15 @@ yoco_status_t run_attn(const void* q, const void* k_cache, const void* v_cache,
         max_blocks_per_req <= 0 || !(scale > 0.f) || max_rows > 0x7fffffff / num_q_heads)
         return YOCO_ERR_INVALID_ARG;
     if (num_reqs == 0 || max_rows == 0) return YOCO_OK;
-    if (!q || !k_cache || !v_cache || !out || !block_table || !seq_lens || !cross_query_start_loc)
-        return YOCO_ERR_INVALID_ARG;
-    if (e4m3 && (page_scales == nullptr || !aligned16(page_scales))) return YOCO_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
-        (workspace && !aligned16(workspace)))
-        return YOCO_ERR_INVALID_ARG;
+    if (!block_table || !seq_lens || !cross_query_start_loc) return YOCO_ERR_INVALID_ARG;
+    if (!plan_only) {
+        if (!q || !k_cache || !v_cache || !out) return YOCO_ERR_INVALID_ARG;
+        if (e4m3 && (page_scales == nullptr || !aligned16(page_scales)))
+            return YOCO_ERR_INVALID_ARG;
+        if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+            return YOCO_ERR_INVALID_ARG;
+    }
+    if (workspace && !aligned16(workspace)) return YOCO_ERR_INVALID_ARG;
     // TMA row coordinates are signed 32-bit
     if (static_cast<int64_t>(num_blocks) * num_kv_heads * block_size > 0x7fffffffll)
         return YOCO_ERR_UNSUPPORTED;
@@ -198,6 +203,7 @@ yoco_status_t run_attn(const void* q, const void* k_cache, const void* v_cache,
     if (!make_plan(dtype, max_rows, num_q_heads, num_kv_heads, head_dim, block_size, max_seq_len,
                    pl))
         return YOCO_ERR_UNSUPPORTED;
+    if (plan_only && !pl.tc) return YOCO_OK;  // the fp32 path plans its split grid on the host
     if (pl.ws_bytes > 0 && (workspace == nullptr || workspace_bytes < pl.ws_bytes))
         return YOCO_ERR_WORKSPACE;
 
@@ -228,16 +234,18 @@ yoco_status_t run_attn(const void* q, const void* k_cache, const void* v_cache,
     p.reverse = (flags & YOCO_ATTN_REVERSE) ? 1 : 0;
     p.overlap = (flags & YOCO_ATTN_OVERLAP) ? 1 : 0;
     p.keep_tail = (flags & YOCO_ATTN_KEEP_TAIL) ? 1 : 0;
+    p.planned = (flags & YOCO_ATTN_PLANNED) ? 1 : 0;
+    p.plan_only = plan_only ? 1 : 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (pl.tc) {
-        p.ws_o = static_cast<float*>(workspace);  // carved up by the launcher
+        p.ws_o = static_cast<float*>(workspace);  // carved up by the kernels (plan first)
         p.ws_ml = nullptr;
-        CUtensorMap mk, mv;
+        CUtensorMap mk = {}, mv = {};
         const int64_t rows = static_cast<int64_t>(num_blocks) * num_kv_heads * block_size;
         const int esz = e4m3 ? 1 : 2;
-        if (!pool_map(&mk, k_cache, rows, head_dim, block_size, esz) ||
-            !pool_map(&mv, v_cache, rows, head_dim, block_size, esz))
+        if (!plan_only && (!pool_map(&mk, k_cache, rows, head_dim, block_size, esz) ||
+                           !pool_map(&mv, v_cache, rows, head_dim, block_size, esz)))
             return cuda_status(cudaErrorInvalidValue);  // descriptor encoding refused
         e = e4m3 ? launch_attn_tc_e4m3(mk, mv, p, head_dim, block_size, device_sm_count(), s)
                  : launch_attn_tc(mk, mv, p, head_dim, block_size, device_sm_count(), s);
@@ -268,6 +276,20 @@ extern "C" yoco_status_t yoco_cross_attn_paged(
                           seq_lens, cross_query_start_loc, num_reqs, max_rows, max_seq_len,
                           num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
                           dtype, flags, workspace, workspace_bytes, err_word, stream);
+}
+
+extern "C" yoco_status_t yoco_cross_attn_plan(
+    const int32_t* block_table, int32_t max_blocks_per_req, const int32_t* seq_lens,
+    const int32_t* cross_query_start_loc, int32_t num_reqs, int32_t max_rows, int32_t max_seq_len,
+    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+    int32_t num_blocks, yoco_dtype_t dtype, uint32_t flags, void* workspace,
+    size_t workspace_bytes, int32_t* err_word, void* stream) {
+    if (flags & ~static_cast<uint32_t>(YOCO_ATTN_OVERLAP)) return YOCO_ERR_INVALID_ARG;
+    return yoco::run_attn(nullptr, nullptr, nullptr, nullptr, nullptr, block_table,
+                          max_blocks_per_req, seq_lens, cross_query_start_loc, num_reqs, max_rows,
+                          max_seq_len, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                          1.0f, dtype, flags, workspace, workspace_bytes, err_word, stream, nullptr,
+                          nullptr, true);
 }
 
 extern "C" yoco_status_t yoco_cross_attn_paged_e4m3(

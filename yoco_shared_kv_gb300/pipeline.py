@@ -146,8 +146,20 @@ class DeviceWorkload:
         N.yoco_select_cross_rows(d["qsl"], d.get("rows_per_req"), ds.row_indices, ds.cqsl,
                                  ds.num_rows, self.err, stream)
 
+    def plan(self, ds: DeviceStep, stream=None, cq: Optional[torch.Tensor] = None) -> None:
+        """The step's attention plan (once per step, after the selection): every layer of
+        the step then reuses it (YOCO_ATTN_PLANNED)."""
+        d = ds.dev
+        wl = self.wl
+        N.yoco_cross_attn_plan(d["block_table"], d["seq_lens"], ds.cqsl if cq is None else cq,
+                               ds.max_seq_len, ds.out.shape[1], wl.num_q_heads, wl.num_kv_heads,
+                               wl.head_dim, wl.block_size, self.k_cache.shape[0],
+                               torch.float8_e4m3fn if self.e4m3 else torch_dtype(wl.dtype),
+                               ds.workspace, self.err, stream)
+
     def attend(self, ds: DeviceStep, layer: int, stream=None, q: Optional[torch.Tensor] = None,
-               out: Optional[torch.Tensor] = None, cq: Optional[torch.Tensor] = None) -> None:
+               out: Optional[torch.Tensor] = None, cq: Optional[torch.Tensor] = None,
+               planned: bool = True) -> None:
         """One cross-decoder layer. Odd layers walk the pages last to first, so each
         layer starts on what the previous one left in L2 (when `alternate` is on).
         Layers after the first overlap their start with the previous layer's end:
@@ -160,6 +172,8 @@ class DeviceWorkload:
             flags |= N.YOCO_ATTN_KEEP_TAIL
         if layer > 0:
             flags |= N.YOCO_ATTN_OVERLAP
+        if planned:  # the step's plan (plan() or the fused step) is in the workspace
+            flags |= N.YOCO_ATTN_PLANNED
         if self.e4m3:
             N.yoco_cross_attn_paged_e4m3(
                 d["q"][layer] if q is None else q, self.k_cache, self.v_cache, self.page_scales,
@@ -197,7 +211,7 @@ class DeviceWorkload:
                                  d["qsl"], ds.max_seq_len, self.wl.scale, ds.workspace, self.err,
                                  stream, flags=N.YOCO_ATTN_KEEP_TAIL if self.alternate else 0)
         for layer in range(1, self.wl.layers if layers is None else layers):
-            self.attend(ds, layer, stream, cq=d["qsl"])
+            self.attend(ds, layer, stream, cq=d["qsl"])  # the step's plan made above
 
     def run_fill(self, stream=None) -> None:
         if self.fill is not None:
@@ -207,9 +221,10 @@ class DeviceWorkload:
         self.run_step_on(self.steps[i], stream, layers)
 
     def run_step_on(self, ds: DeviceStep, stream=None, layers: Optional[int] = None) -> None:
-        """append -> select -> every cross-decoder layer, all enqueued on one stream."""
+        """append -> select -> plan -> every cross-decoder layer, all on one stream."""
         self.append(ds, stream)
         self.select(ds, stream)
+        self.plan(ds, stream)
         for layer in range(self.wl.layers if layers is None else layers):
             self.attend(ds, layer, stream)
 
