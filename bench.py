@@ -48,7 +48,8 @@ def parse_args(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--config", type=int, default=1, help="workload index 0..4 (1 = pure decode)")
+    ap.add_argument("--config", type=int, default=1,
+                    help="workload index 0..4 (1 = pure decode); 5 = speculative verification")
     ap.add_argument("--reqs", type=int, default=None, help="smaller case: override request count")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
@@ -79,7 +80,7 @@ def dist_env():
 def make_workload(config: int, rank: int = 0, reqs=None, seed_offset: int = 0):
     """Replica `rank` of workload `config`: same shapes, its own seed."""
     import workloads as W
-    base = {0: 1000, 1: 1001, 2: 1002, 3: 1003, 4: 1004}[config] + 7919 * (rank + seed_offset)
+    base = {0: 1000, 1: 1001, 2: 1002, 3: 1003, 4: 1004, 5: 1006}[config] + 7919 * (rank + seed_offset)
     if config == 0:
         return W.toy_r1r2(base)
     if config == 1:
@@ -88,6 +89,8 @@ def make_workload(config: int, rank: int = 0, reqs=None, seed_offset: int = 0):
         return W.mixed_step(base, **({} if reqs is None else {"n_decode": reqs}))
     if config == 3:
         return W.long_context(base, **({} if reqs is None else {"num_reqs": reqs}))
+    if config == 5:  # beyond the five: speculative verification, 4 rows per request
+        return W.spec_decode(base, **({} if reqs is None else {"num_reqs": reqs}))
     return W.shared_prefix(base, **({} if reqs is None else {"num_reqs": reqs}))
 
 
@@ -585,6 +588,12 @@ def run_ours(args, rank, world, local):
             fu[kv] = {"workload": r["config"]["workload"], "ms_per_step": r["ms_per_step"],
                       "value": r["value"], "query_rows_per_s": r["query_rows_per_s"]}
         res["fused_decode_step"] = fu
+        # beyond the five: speculative verification (4 cross rows per request) at
+        # the pure-decode shapes
+        r = measure(args, 5, rank, world, local, steps=sub_steps, warmup=sub_warm, e2e=False,
+                    cold=not args.no_cold)
+        r.pop("_wl"), r.pop("_step_i")
+        res["multi_row"] = _compact(r)
     res["clocks"] = sampler.stop() if sampler else None
     return res
 

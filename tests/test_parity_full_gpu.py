@@ -109,3 +109,28 @@ def test_full_size_fused_decode_step(P, kv):
     assert torch.equal(a.k_cache.view(torch.uint8), b.k_cache.view(torch.uint8))
     assert torch.equal(a.v_cache.view(torch.uint8), b.v_cache.view(torch.uint8))
     assert torch.equal(a.steps[0].out.view(torch.int16), b.steps[0].out.view(torch.int16))
+
+
+def test_full_size_speculative_rows(P):
+    """Speculative verification at the pure-decode shapes (64 requests x 4 rows):
+    selection bit-exact, attention on sampled rows x layers against the oracle."""
+    from workloads import MULTI_ROW_FULL
+    wl = MULTI_ROW_FULL()
+    dw = P.DeviceWorkload(wl)
+    dw.run_fill()
+    dw.run_step(0)
+    torch.cuda.synchronize()
+    assert dw.error_bits() == 0
+    step = wl.steps[0]
+    ds = dw.steps[0]
+    o_rows, o_cq, n = oracle.select_cross_rows(step.query_start_loc, step.rows_per_req)
+    assert n == step.rows_upper == 256
+    assert np.array_equal(ds.row_indices.cpu().numpy()[:n], o_rows)
+    assert np.array_equal(ds.cqsl.cpu().numpy(), o_cq)
+    got = gpu_out(ds.out)
+    assert np.isfinite(got).all()
+    rng = np.random.default_rng(55)
+    rows = sorted(set([0, 1, 2, 3, n - 1] + rng.choice(n, size=4, replace=False).tolist()))
+    layers = [0, wl.layers - 1]
+    ref = oracle_step_out(wl, step, layers=layers, rows=rows)
+    assert np.abs(got[layers][:, rows] - ref).max() <= ATOL["bf16"]

@@ -474,3 +474,16 @@ def test_plan_is_reused_across_layers_and_replaced_per_step(P):
         got = gpu_out(dw.steps[i].out[:, :n])
         ref = oracle_step_out(wl, step)
         assert np.abs(got - ref).max() <= ATOL["bf16"], i
+
+
+def test_speculative_rows_small_against_oracle(P):
+    """Speculative verification: every request asks for its 4 trailing rows, each
+    with its own bottom-right causal length (all rows, every layer)."""
+    from workloads import MULTI_ROW_SMALL
+    wl = MULTI_ROW_SMALL()
+    dw = P.DeviceWorkload(wl)
+    dw.run_all()
+    torch.cuda.synchronize()
+    assert dw.error_bits() == 0
+    ref = oracle_step_out(wl, wl.steps[0])
+    assert np.abs(gpu_out(dw.steps[0].out) - ref).max() <= ATOL["bf16"]

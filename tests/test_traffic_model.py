@@ -50,7 +50,8 @@ def test_model_counts_rows_like_selection(N):
 
 def test_model_predicts_measured_dram_bytes(N):
     """profiles/traffic.txt holds ncu DRAM bytes per attention launch at full size; a launch
-    measured alone (caches flushed, no reuse between layers) moves what the model predicts."""
+    measured alone (caches flushed, no reuse between layers) reads what the model predicts
+    (its writes add the workspace partials of the cross-CTA merge, ~1% of the bytes)."""
     import bench
     lines = open(os.path.join(ROOT, "profiles", "traffic.txt")).read().splitlines()
     meas = dict(l.split("=", 1) for l in lines if "=" in l and not l.startswith("#"))
@@ -65,7 +66,8 @@ def test_model_predicts_measured_dram_bytes(N):
                                             wl.head_dim, wl.block_size, dt)
         per_layer = tot / wl.layers
         assert per_layer == bench.accounting(wl, st, e4m3)["attn_bytes_layer"]
-        assert abs(float(meas[name + "_isolated"]) / per_layer - 1.0) < 0.006, name  # within 0.6 %
+        assert abs(float(meas[name + "_isolated_read"]) / per_layer - 1.0) < 0.006, name  # within 0.6 %
+        assert float(meas[name + "_isolated"]) / per_layer < 1.015, name  # partials: < 1.5 % more
         # inside the layer sequence part of it comes from L2 (layers alternate walk direction)
         assert float(meas[name]) < float(meas[name + "_isolated"])
 

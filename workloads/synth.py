@@ -357,6 +357,24 @@ def shared_prefix(seed: int = 1004, num_reqs: int = 256, prefix_len: int = 4096,
                  description=f"shared prefix {prefix_len} + tails U[{tail_lo},{tail_hi}] x {num_reqs}")
 
 
+def spec_decode(seed: int = 1006, num_reqs: int = 64, ctx_lo: int = 1024, ctx_hi: int = 8192,
+                draft: int = 4, H_q: int = 8, H_kv: int = 2, D: int = 256, bs: int = 16,
+                layers: int = 10, dtype: str = "bf16") -> Workload:
+    """Speculative verification at the pure-decode shapes: every request schedules
+    `draft` tokens (the draft to verify) and asks for all of them as cross rows
+    ("You Only Cache Once, in vLLM": the metadata builder gives a request several
+    rows); contexts uniform in [lo, hi] before the draft."""
+    rng = np.random.default_rng([seed, 3])
+    ctx = [int(x) for x in rng.integers(ctx_lo, ctx_hi, size=num_reqs, endpoint=True)]
+    lens = [c + draft for c in ctx]
+    entries = [(r, n, draft) for r, n in enumerate(lens)]
+    return _make(f"spec_decode_{dtype}", dtype=dtype, H_q=H_q, H_kv=H_kv, D=D, bs=bs,
+                 layers=layers, seed=seed, full_lens=lens, step_entries=entries,
+                 rows_per_req=[draft] * num_reqs,
+                 description=f"speculative verification: {num_reqs} requests x {draft} rows, "
+                             f"ctx U[{ctx_lo},{ctx_hi}]")
+
+
 def chunked_prefill_spec(seed: int = 1005, H_q: int = 8, H_kv: int = 2, D: int = 128, bs: int = 16,
                          layers: int = 3, dtype: str = "bf16") -> Workload:
     """Three scheduling steps mixing a chunked prefill, a decode and a speculative decode.
@@ -413,6 +431,11 @@ SMALL = {
     3: lambda: long_context(2003, num_reqs=2, ctx=3000, layers=3),
     4: lambda: shared_prefix(2004, num_reqs=5, prefix_len=256, tail_lo=1, tail_hi=70, layers=3),
 }
+
+# Beyond the five: speculative verification (several cross rows per request)
+# at the pure-decode shapes, full size and scaled down.
+MULTI_ROW_FULL = lambda: spec_decode(1006)  # noqa: E731
+MULTI_ROW_SMALL = lambda: spec_decode(2006, num_reqs=5, ctx_lo=1, ctx_hi=900, layers=2)  # noqa: E731
 
 
 def page_scales(wl: Workload, lo: float = 3.5, hi: float = 5.0) -> np.ndarray:
