@@ -201,6 +201,12 @@ size_t yoco_cross_attn_workspace_size(int32_t max_rows, int32_t num_q_heads, int
  *                          written into it by yoco_cross_attn_plan or by a call without
  *                          PLANNED). One workspace serves one stream at a time.
  *   err_word               device int32 or NULL
+ * Several cross rows of one request (max_rows > num_reqs: chunked prefill,
+ * speculative verification) with at most 4 query heads per kv head are
+ * walked together on the bf16 and e4m3 paths: 8 / G consecutive rows of a
+ * request share one pass over its pages (the group's last row's causal end),
+ * each row masked at its own end, so the cache is read once per group, not
+ * once per row. Each row's result equals its own walk up to summation order.
  * Long contexts are split across CTAs and merged with a log-sum-exp
  * combine in a fixed split order, so results do not depend on where pages
  * sit in the pool. Accuracy: fp32 accumulation; bf16 probabilities feed the

@@ -211,3 +211,15 @@ def test_fused_step_bad_page_flagged(P, N, kv):
     # nothing was written for the skipped token; the other requests' tokens were
     changed = (dw.k_cache.view(torch.uint8) != before.view(torch.uint8))
     assert changed.any()
+
+
+@pytest.mark.parametrize("H_q,H_kv,D,bs,draft", [(8, 2, 256, 16, 4), (4, 2, 128, 32, 3)])
+def test_e4m3_row_groups(P, H_q, H_kv, D, bs, draft):
+    """Several cross rows per request over the e4m3 cache: rows grouped on one walk."""
+    from workloads import spec_decode
+    wl = spec_decode(7400 + H_q + draft, num_reqs=5, ctx_lo=1, ctx_hi=700, draft=draft, H_q=H_q,
+                     H_kv=H_kv, D=D, bs=bs, layers=2)
+    scales = page_scales(wl)
+    dw = _run(P, wl, scales)
+    assert dw.error_bits() == 0
+    _check_steps(wl, dw, scales, layers=[0, 1])

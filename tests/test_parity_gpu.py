@@ -487,3 +487,88 @@ def test_speculative_rows_small_against_oracle(P):
     assert dw.error_bits() == 0
     ref = oracle_step_out(wl, wl.steps[0])
     assert np.abs(gpu_out(dw.steps[0].out) - ref).max() <= ATOL["bf16"]
+
+
+@pytest.mark.parametrize("H_q,H_kv,D,bs,draft", [(8, 2, 256, 16, 4), (4, 4, 128, 32, 3),
+                                                 (2, 2, 64, 16, 7), (3, 1, 128, 16, 5),
+                                                 (16, 1, 128, 32, 2)])
+def test_row_groups_against_oracle_and_page_permutation(P, H_q, H_kv, D, bs, draft):
+    """Several cross rows per request (max_rows above num_reqs): rows of a request
+    share one walk over its pages in groups (groups of up to 4 heads: 8 / G rows per
+    group), each row with its own causal end. Every row of every layer against the
+    oracle, and bit-identical under a re-permutation of the physical pages."""
+    from workloads import spec_decode
+    seed = 7100 + H_q * 13 + D + draft
+    a = spec_decode(seed, num_reqs=5, ctx_lo=1, ctx_hi=700, draft=draft, H_q=H_q, H_kv=H_kv,
+                    D=D, bs=bs, layers=2)
+    b = spec_decode(seed, num_reqs=5, ctx_lo=1, ctx_hi=700, draft=draft, H_q=H_q, H_kv=H_kv,
+                    D=D, bs=bs, layers=2)
+    perm = np.random.default_rng(seed).permutation(b.num_blocks).astype(np.int32)
+    for st in [b.fill] + b.steps:
+        st.block_table = perm[st.block_table]
+    outs = []
+    for wl in (a, b):
+        dw = P.DeviceWorkload(wl, alternate=True)  # odd layers walk backwards
+        dw.run_all()
+        torch.cuda.synchronize()
+        assert dw.error_bits() == 0
+        outs.append(dw.steps[0].out.cpu())
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    ref = oracle_step_out(a, a.steps[0])
+    assert np.abs(outs[0].float().numpy().astype(np.float64) - ref).max() <= ATOL["bf16"]
+
+
+def test_grouped_and_single_row_walks_agree(P, N):
+    """The same speculative batch with max_rows = num_reqs + its rows (rows grouped on
+    one walk) and, with the rows spread one per request (no grouping): both within
+    tolerance of the oracle."""
+    from workloads import spec_decode
+    wl = spec_decode(7300, num_reqs=4, ctx_lo=30, ctx_hi=500, draft=4, layers=1)
+    dw = P.DeviceWorkload(wl)
+    dw.run_all()
+    torch.cuda.synchronize()
+    assert dw.error_bits() == 0
+    ref = oracle_step_out(wl, wl.steps[0])[0]
+    assert np.abs(gpu_out(dw.steps[0].out[0]) - ref).max() <= ATOL["bf16"]
+    # one row per request: request r's four rows become four one-row requests with the
+    # same pages and causal ends (seq_len - 3 .. seq_len), so max_rows == num_reqs
+    st = wl.steps[0]
+    ds = dw.steps[0]
+    R = st.num_reqs
+    bt = np.repeat(np.asarray(st.block_table), 4, axis=0)
+    sl = np.concatenate([np.asarray(st.seq_lens)[r] - 3 + np.arange(4) for r in range(R)])
+    cq = np.arange(4 * R + 1)
+    out = torch.full_like(ds.out[0], float("nan"))
+    N.yoco_cross_attn_paged(ds.dev["q"][0], dw.k_cache, dw.v_cache, out, _i32(bt),
+                            _i32(sl.astype(np.int32)), _i32(cq), ds.max_seq_len, wl.scale,
+                            ds.workspace, dw.err)
+    torch.cuda.synchronize()
+    assert dw.error_bits() == 0
+    assert np.abs(gpu_out(out) - ref).max() <= ATOL["bf16"]
+
+
+def test_row_group_with_an_empty_row(P, N):
+    """A request whose seq_len is below its row count: its first row has no key and
+    shares a group with rows that have keys. That row is zero-filled and flagged
+    EMPTY_ROW; the others match the oracle's rows with keys."""
+    from workloads import spec_decode
+    wl = spec_decode(7500, num_reqs=3, ctx_lo=20, ctx_hi=200, draft=4, layers=1)
+    dw = P.DeviceWorkload(wl)
+    dw.run_all()
+    torch.cuda.synchronize()
+    ds = dw.steps[0]
+    sl = ds.dev["seq_lens"].clone()
+    sl[1] = 3  # request 1 has 4 rows: keys 0, 1, 2, 3 -> its first row has none
+    out = torch.full_like(ds.out[0], 5.0)
+    dw.err.zero_()
+    N.yoco_cross_attn_paged(ds.dev["q"][0], dw.k_cache, dw.v_cache, out, ds.dev["block_table"],
+                            sl, ds.cqsl, ds.max_seq_len, wl.scale, ds.workspace, dw.err)
+    torch.cuda.synchronize()
+    assert dw.error_bits() == N.DEVERR_EMPTY_ROW
+    got = gpu_out(out)
+    assert (got[4] == 0).all()  # request 1's first row
+    assert np.isfinite(got).all()
+    import dataclasses
+    st = dataclasses.replace(wl.steps[0], seq_lens=sl.cpu().numpy())
+    ref = oracle_step_out(wl, st, layers=[0], rows=[r for r in range(12) if r != 4])[0]
+    assert np.abs(np.delete(got, 4, axis=0) - ref).max() <= ATOL["bf16"]

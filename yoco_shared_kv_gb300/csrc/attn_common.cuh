@@ -36,6 +36,8 @@ struct AttnParams {
     int32_t reverse;            // tensor-core path: walk each worker's pages from the end
     int32_t overlap;            // tensor-core path: launch as a programmatic dependent
     int32_t keep_tail;          // tensor-core path: L2 hints, keep this walk's tail for the next layer
+    int32_t rg;                 // tensor-core path: cross rows of a request grouped on one walk (1: none)
+    int32_t vhs;                // tensor-core path: virtual heads (group rows x heads) per partial slot
     int32_t planned;            // tensor-core path: the workspace already holds this step's plan
     int32_t plan_only;          // tensor-core path: make the plan, launch no attention
 };

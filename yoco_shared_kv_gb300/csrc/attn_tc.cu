@@ -27,7 +27,9 @@ size_t tc_workspace_bytes(int sms, int H_kv, int G, int D, int BS, bool e4m3) {
     const bool wide = G > 8;  // two 8-head tiles
     const int nw = e4m3 ? (wide ? nw_of<true, 2>(D, BS) : nw_of<true, 1>(D, BS))
                         : (wide ? nw_of<false, 2>(D, BS) : nw_of<false, 1>(D, BS));
-    const size_t pieces = static_cast<size_t>(tc_pieces(ctas, nw, G));
+    // a partial slot holds the G heads of one row, or the 8 virtual heads of a
+    // group of rows sharing one walk: max(G, 8) covers both
+    const size_t pieces = static_cast<size_t>(tc_pieces(ctas, nw, G > 8 ? G : 8));
     return static_cast<size_t>(tc_plan_bytes(ctas, nw)) + pieces * (static_cast<size_t>(D) * 4 + 8);
 }
 

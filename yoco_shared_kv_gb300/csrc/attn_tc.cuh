@@ -109,12 +109,22 @@ __device__ __forceinline__ int32_t row_pages(int32_t kv_len, int32_t cap, int32_
     return (kv_len + bs - 1) / bs;
 }
 
-// Pages (all kv heads) of request r's cross rows below max_rows.
+// Rows of a request are taken in groups of up to p.rg consecutive rows (below
+// max_rows); a group's rows share one walk over the request's pages, up to the
+// last row's causal end. Keys of the group's last row: row n of a request with
+// k rows starting at c0 sees seq - k + (n - c0) + 1 keys.
+__device__ __forceinline__ int32_t group_kv(int32_t seq, int32_t k, int32_t c0, int32_t n,
+                                            int32_t nr) {
+    return seq - k + (n + nr - c0);
+}
+
+// Pages (all kv heads) of request r's cross-row groups below max_rows.
 __device__ __forceinline__ int64_t req_pages(const AttnParams& p, int32_t r, int32_t cap) {
     const int32_t c0 = __ldg(p.cqsl + r), c1 = __ldg(p.cqsl + r + 1);
     const int32_t k = c1 - c0, hi = min(c1, p.max_rows), seq = __ldg(p.seq_lens + r);
     int64_t s = 0;
-    for (int32_t n = c0; n < hi; ++n) s += row_pages(seq - k + (n - c0) + 1, cap, p.block_size);
+    for (int32_t n = c0; n < hi; n += p.rg)
+        s += row_pages(group_kv(seq, k, c0, n, min(p.rg, hi - n)), cap, p.block_size);
     return s * p.H_kv;
 }
 
@@ -146,7 +156,8 @@ __device__ int64_t total_pages(const AttnParams& p, int lane, int32_t cap) {
 // Position in the flattened (row, kv head, page) sequence.
 struct Cursor {
     int64_t seg_start;  // flattened index of the segment's first page
-    int32_t req, n, g, pp, kv_len, pages;
+    int32_t req, n, g, pp, kv_len, pages;  // n: first row of the group, kv_len: its last row's keys
+    int32_t nr;                            // rows in the group
 };
 
 // Cursor of flattened page x (< total). Warp-collective; all lanes agree.
@@ -164,15 +175,17 @@ __device__ void locate(const AttnParams& p, int lane, int64_t x, int32_t cap, Cu
             int64_t off = done + __shfl_sync(0xffffffffu, incl - v, src);
             const int32_t req = base + src;
             const int32_t c0 = __ldg(p.cqsl + req), c1 = __ldg(p.cqsl + req + 1);
-            const int32_t k = c1 - c0, seq = __ldg(p.seq_lens + req);
-            for (int32_t n = c0; n < c1 && n < p.max_rows; ++n) {
-                const int32_t kv = seq - k + (n - c0) + 1;
+            const int32_t k = c1 - c0, seq = __ldg(p.seq_lens + req), hi = min(c1, p.max_rows);
+            for (int32_t n = c0; n < hi; n += p.rg) {
+                const int32_t nr = min(p.rg, hi - n);
+                const int32_t kv = group_kv(seq, k, c0, n, nr);
                 const int32_t pg = row_pages(kv, cap, p.block_size);
                 const int64_t seg_pages = static_cast<int64_t>(pg) * p.H_kv;
                 if (x < off + seg_pages) {
                     const int64_t rel = x - off;
                     c.req = req;
                     c.n = n;
+                    c.nr = nr;
                     c.kv_len = min(kv, cap);
                     c.pages = pg;
                     c.g = static_cast<int32_t>(rel / pg);
@@ -188,7 +201,9 @@ __device__ void locate(const AttnParams& p, int lane, int64_t x, int32_t cap, Cu
     }
 }
 
-// Next page in the flattened order (skips rows without keys).
+// Next page in the flattened order (skips groups without keys). RG = false:
+// the launch has no row groups (p.rg == 1, every group one row).
+template <bool RG = true>
 __device__ __forceinline__ void advance(const AttnParams& p, Cursor& c, int32_t cap) {
     if (++c.pp < c.pages) return;
     c.seg_start += c.pages;
@@ -196,18 +211,22 @@ __device__ __forceinline__ void advance(const AttnParams& p, Cursor& c, int32_t 
     if (++c.g < p.H_kv) return;
     c.g = 0;
     for (;;) {
-        if (++c.n >= p.max_rows) return;
+        c.n += RG ? c.nr : 1;
+        if (c.n >= p.max_rows) return;
         while (c.req + 1 < p.num_reqs && __ldg(p.cqsl + c.req + 1) <= c.n) ++c.req;
         const int32_t c0 = __ldg(p.cqsl + c.req), c1 = __ldg(p.cqsl + c.req + 1);
         if (c.n >= c1) return;
-        const int32_t kv = __ldg(p.seq_lens + c.req) - (c1 - c0) + (c.n - c0) + 1;
+        // groups start at c0, c0 + rg, ...: c.n is the next one of this request
+        if (RG) c.nr = min(p.rg, min(c1, p.max_rows) - c.n);
+        const int32_t kv = group_kv(__ldg(p.seq_lens + c.req), c1 - c0, c0, c.n, RG ? c.nr : 1);
         c.pages = row_pages(kv, cap, p.block_size);
         c.kv_len = min(kv, cap);
         if (c.pages > 0) return;
     }
 }
 
-// Previous page in the flattened order (skips rows without keys).
+// Previous page in the flattened order (skips groups without keys).
+template <bool RG = true>
 __device__ __forceinline__ void retreat(const AttnParams& p, Cursor& c, int32_t cap) {
     if (--c.pp >= 0) return;
     if (--c.g >= 0) {  // same row, previous kv head
@@ -216,10 +235,18 @@ __device__ __forceinline__ void retreat(const AttnParams& p, Cursor& c, int32_t 
         return;
     }
     for (;;) {
-        if (--c.n < 0) return;
-        while (c.req > 0 && __ldg(p.cqsl + c.req) > c.n) --c.req;
+        // the group ending at row c.n - 1
+        const int32_t x = c.n - 1;
+        if (x < 0) return;
+        while (c.req > 0 && __ldg(p.cqsl + c.req) > x) --c.req;
         const int32_t c0 = __ldg(p.cqsl + c.req), c1 = __ldg(p.cqsl + c.req + 1);
-        const int32_t kv = __ldg(p.seq_lens + c.req) - (c1 - c0) + (c.n - c0) + 1;
+        if (RG) {
+            c.n = c0 + (x - c0) / p.rg * p.rg;
+            c.nr = min(p.rg, min(c1, p.max_rows) - c.n);
+        } else {
+            c.n = x;
+        }
+        const int32_t kv = group_kv(__ldg(p.seq_lens + c.req), c1 - c0, c0, c.n, RG ? c.nr : 1);
         const int32_t pg = row_pages(kv, cap, p.block_size);
         if (pg > 0) {
             c.pages = pg;
@@ -242,9 +269,9 @@ constexpr int kMaxCtas = 1024;
 
 struct PieceHdr {
     int64_t s0, s1;    // segment [first page, end) in the flattened order
-    const float* o;    // [G][D] partial output: in the warp's ring or in the workspace
-    const float2* ml;  // [G] (m, l)
-    int32_t n, g;
+    const float* o;    // [virtual heads][D] partial output: in the warp's ring or in the workspace
+    const float2* ml;  // [virtual heads] (m, l)
+    int32_t n, g, nr;  // first row, kv head, rows of the group
     int32_t valid;
 };
 
@@ -264,7 +291,7 @@ constexpr uint32_t kPlanMagic = 0x594f434fu;
 struct __align__(16) WarpPlan {
     int64_t P;          // pages of the launch
     int64_t seg_start;  // cursor of the walk's first page (see Cursor)
-    int32_t req, n, g, pp, kv_len, pages;
+    int32_t req, n, g, pp, kv_len, pages;  // g: kv head | (rows of the group << 16)
     int32_t blk[kPlanBlk];  // block-table entries of the walk's first pages
 };
 static_assert(sizeof(WarpPlan) == 64, "one plan record is four 16-byte loads");
@@ -273,7 +300,8 @@ static_assert(sizeof(WarpPlan) == 64, "one plan record is four 16-byte loads");
 struct __align__(16) PlanHdr {
     uint32_t magic;
     int32_t num_reqs, max_rows, H_kv, G, block_size, max_blocks, nw, ctas, stages, d;
-    int32_t pad[5];
+    int32_t rg;
+    int32_t pad[4];
 };
 static_assert(sizeof(PlanHdr) == 64, "plan header size");
 
@@ -283,8 +311,9 @@ struct __align__(16) CtaHdr {
     int64_t P;       // pages of the launch
     int64_t a0, a1;  // segment of the first page [first, end); a0 < 0: slice starts past the end
     int64_t b0, b1;  // segment of the last page; b0 < 0: empty slice
-    int32_t an, ag;  // (row, kv head) of segment a
-    int32_t bn, bg;  // (row, kv head) of segment b
+    int32_t an, ag;  // (first row, kv head) of segment a
+    int32_t bn, bg;  // (first row, kv head) of segment b
+    int32_t anr, bnr;  // rows of the groups of segments a and b
 };
 static_assert(sizeof(CtaHdr) == 64, "CTA header size");
 
@@ -322,11 +351,11 @@ __device__ __forceinline__ TcWs tc_ws(const AttnParams& p, int ctas, int nw, int
     w.hdr = reinterpret_cast<CtaHdr*>(w.wplan + 2ll * ctas * nw);
     w.cnt = reinterpret_cast<uint32_t*>(w.hdr + ctas);
     float* o = reinterpret_cast<float*>(base + tc_plan_bytes(ctas, nw));
-    const int64_t per = 2ll * p.G;  // pieces per worker (first / last segment) x heads
+    const int64_t per = 2ll * p.vhs;  // pieces per worker (first / last segment) x virtual heads
     const int64_t W = static_cast<int64_t>(ctas) * nw;
     w.w_o = o;
     w.c_o = o + W * per * D;
-    w.w_ml = reinterpret_cast<float2*>(o + tc_pieces(ctas, nw, p.G) * D);
+    w.w_ml = reinterpret_cast<float2*>(o + tc_pieces(ctas, nw, p.vhs) * D);
     w.c_ml = w.w_ml + W * per;
     return w;
 }
@@ -335,7 +364,7 @@ __device__ __forceinline__ bool plan_matches(const PlanHdr& h, const AttnParams&
                                              int BS, int nw, int stages, int ctas) {
     return h.magic == kPlanMagic && h.num_reqs == p.num_reqs && h.max_rows == p.max_rows &&
            h.H_kv == p.H_kv && h.G == p.G && h.block_size == BS && h.max_blocks == p.max_blocks &&
-           h.nw == nw && h.ctas == ctas && h.stages == stages && h.d == D;
+           h.nw == nw && h.ctas == ctas && h.stages == stages && h.d == D && h.rg == p.rg;
 }
 
 // Cursor of the first page of a walk over flattened pages [lo, hi) (forward:
@@ -347,6 +376,7 @@ __device__ void plan_walk(const AttnParams& p, int lane, int64_t P, int64_t lo, 
     c.req = -1;
     c.seg_start = 0;
     c.n = c.g = c.pp = c.kv_len = c.pages = 0;
+    c.nr = 1;
     int32_t blk[kPlanBlk];
 #pragma unroll
     for (int i = 0; i < kPlanBlk; ++i) blk[i] = -1;
@@ -369,7 +399,7 @@ __device__ void plan_walk(const AttnParams& p, int lane, int64_t P, int64_t lo, 
         out->seg_start = c.seg_start;
         out->req = c.req;
         out->n = c.n;
-        out->g = c.g;
+        out->g = c.g | (c.nr << 16);  // kv head, and the rows of the group above it
         out->pp = c.pp;
         out->kv_len = c.kv_len;
         out->pages = c.pages;
@@ -395,7 +425,7 @@ __global__ void __launch_bounds__(NW * 32) attn_tc_plan(const AttnParams p) {
     const int64_t my_hi = cta_lo + (cta_hi - cta_lo) * (warp + 1) / NW;
     // header fields: warp 0 the segment of page cta_lo, warp 1 that of page cta_hi - 1
     int64_t hs0 = -1, hs1 = -1;
-    int32_t hn = 0, hg = 0;
+    int32_t hn = 0, hg = 0, hnr = 1;
     if (warp <= 1) {
         const int64_t x = warp == 0 ? cta_lo : cta_hi - 1;
         const bool any = warp == 0 ? cta_lo < P : cta_hi > cta_lo;
@@ -407,6 +437,7 @@ __global__ void __launch_bounds__(NW * 32) attn_tc_plan(const AttnParams p) {
                 hs1 = h.seg_start + h.pages;
                 hn = h.n;
                 hg = h.g;
+                hnr = h.nr;
             }
         }
     }
@@ -422,11 +453,13 @@ __global__ void __launch_bounds__(NW * 32) attn_tc_plan(const AttnParams p) {
             hp->a1 = hs1;
             hp->an = hn;
             hp->ag = hg;
+            hp->anr = hnr;
         } else {
             hp->b0 = hs0;
             hp->b1 = hs1;
             hp->bn = hn;
             hp->bg = hg;
+            hp->bnr = hnr;
         }
     }
     if (threadIdx.x == 0) {
@@ -444,6 +477,7 @@ __global__ void __launch_bounds__(NW * 32) attn_tc_plan(const AttnParams p) {
             h.ctas = static_cast<int32_t>(C);
             h.stages = STAGES;
             h.d = D;
+            h.rg = p.rg;
             *ws.plan = h;
         }
     }
@@ -507,14 +541,14 @@ __host__ __device__ __forceinline__ int merge_scratch_floats(int ctas, int G, in
     return (G * D + 10 * ctas + 14 * (G + 1) + 4 + 3) & ~3;
 }
 
-template <int D>
+template <int D, bool RG>
 __device__ __forceinline__ void cross_cta_merge(const AttnParams& p, const TcWs& ws,
                                                 const CtaHdr& Hc, float* scratch) {
     const int32_t c = blockIdx.x, ctas = gridDim.x;
     const int nthr = static_cast<int>(blockDim.x);
     const int64_t P = Hc.P;
     if (P <= 0) return;
-    const int G = p.G;
+    const int G = p.G, VS = p.vhs;  // heads of a kv group; virtual heads per partial slot
     if (!(P * c / ctas < P * (c + 1) / ctas)) return;  // a CTA without pages holds no partial
 
     // The (at most two) cut segments: {first page, row, kv head, first CTA,
@@ -523,7 +557,7 @@ __device__ __forceinline__ void cross_cta_merge(const AttnParams& p, const TcWs&
     // exactly one page of the segment and holder j owns page s0 + j.
     struct Seg {
         int64_t s0;
-        int32_t n, g, cf, nsh, rank;
+        int32_t n, g, nr, cf, nsh, rank;
     };
     Seg sg0 = {}, sg1 = {};
     int nseg = 0;
@@ -539,6 +573,7 @@ __device__ __forceinline__ void cross_cta_merge(const AttnParams& p, const TcWs&
         x.s0 = s0;
         x.n = which == 0 ? Hc.an : Hc.bn;
         x.g = which == 0 ? Hc.ag : Hc.bg;
+        x.nr = which == 0 ? Hc.anr : Hc.bnr;
         x.cf = c_first;
         x.nsh = dense ? c_last - c_first + 1 : static_cast<int32_t>(s1 - s0);
         x.rank = dense ? c - c_first : static_cast<int32_t>(P * c / ctas - s0);
@@ -571,14 +606,14 @@ __device__ __forceinline__ void cross_cta_merge(const AttnParams& p, const TcWs&
     const int tl = static_cast<int>(threadIdx.x) - si * half;  // thread index within the half
     const Seg sg = si == 0 ? sg0 : sg1;
     const int nh_ = sg.nsh;
-    // this CTA's share of the segment's G x D outputs (whole 16-byte vectors),
-    // and the heads it touches
-    const int total = G * D;
+    // this CTA's share of the segment's (rows x G) x D outputs (whole 16-byte
+    // vectors), and the virtual heads (row-major over the group's rows) it touches
+    const int total = (RG ? sg.nr : 1) * G * D;
     const int per = ((total + nh_ - 1) / nh_ + 3) & ~3;
     const int lo = min(total, sg.rank * per), hi = min(total, lo + per);
     const int nout = hi - lo, nv = nout >> 2;
     const int h_lo = lo / D, nhd = nout > 0 ? (hi - 1) / D - h_lo + 1 : 0;
-    float* so = scratch + 16 + si * merge_scratch_floats(ctas, G, D);  // [holder][nout]
+    float* so = scratch + 16 + si * merge_scratch_floats(ctas, VS, D);  // [holder][nout]
     float2* sml = reinterpret_cast<float2*>(so + nh_ * nout);          // [holder][nhd]
     float* sf = reinterpret_cast<float*>(sml + nh_ * nhd);             // [holder][nhd] 2^(m - M)
     float* sInvL = sf + nh_ * nhd;                                     // [nhd]
@@ -586,7 +621,7 @@ __device__ __forceinline__ void cross_cta_merge(const AttnParams& p, const TcWs&
     // for every other holder it is the first segment (slot 0)
     auto slot = [&](int j) -> int64_t {
         const int64_t cj = dense ? sg.cf + j : owner(sg.s0 + j, P, ctas);
-        return (cj * 2 + (j == 0 ? 1 : 0)) * G;
+        return (cj * 2 + (j == 0 ? 1 : 0)) * VS;
     };
     // One round of asynchronous global -> shared copies: every holder's
     // outputs of the share (16-byte vectors) and (m, l) of its heads. The
@@ -629,7 +664,6 @@ __device__ __forceinline__ void cross_cta_merge(const AttnParams& p, const TcWs&
     }
     __syncthreads();
     __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out);
-    const int64_t head0 = static_cast<int64_t>(sg.n) * p.H_q + sg.g * G;
     // a holder with no key has f = 0 and a slot never written: select, not 0 * x
     auto term = [&](int j, int e, int hh) {
         const float f = sf[j * nhd + hh];
@@ -650,7 +684,14 @@ __device__ __forceinline__ void cross_cta_merge(const AttnParams& p, const TcWs&
         }
 #pragma unroll 1
         for (; j < nh_; ++j) a0 += term(j, e, hh);
-        outp[head0 * D + lo + e] = __float2bfloat16_rn(((a0 + a1) + (a2 + a3)) * sInvL[hh]);
+        int64_t dst = (static_cast<int64_t>(sg.n) * p.H_q + sg.g * G) * D + lo + e;
+        if constexpr (RG) {
+            if (!(sInvL[hh] < INFINITY)) continue;  // a group row without keys: zero-filled in the kernel
+            // virtual head v = (row of the group) * G + head
+            const int v = (lo + e) / D, d = lo + e - v * D;
+            dst = ((static_cast<int64_t>(sg.n) + v / G) * p.H_q + sg.g * G + v % G) * D + d;
+        }
+        outp[dst] = __float2bfloat16_rn(((a0 + a1) + (a2 + a3)) * sInvL[hh]);
     }
 }
 
@@ -658,7 +699,10 @@ __device__ __forceinline__ void cross_cta_merge(const AttnParams& p, const TcWs&
 
 // FUSE: fused decode step (append this step's tokens, patch them into the
 // copied pages); instantiated with REV = false only.
-template <int D, int BS, int NT, bool REV, bool F8, bool FUSE>
+// RG: cross rows grouped on one walk (p.rg > 1; NT = 1 and FUSE = false only).
+// Without it every segment is one row and the per-column causal masks and
+// the guard for columns without keys compile away.
+template <int D, int BS, int NT, bool REV, bool F8, bool FUSE, bool RG>
 __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
     attn_tc_persistent(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
@@ -667,6 +711,7 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
     static_assert(S::PIECE_PAIR <= STAGES * S::STAGE_BYTES,
                   "a warp's two end-of-slice pieces must fit in its ring");
     static_assert(!F8 || D % 128 == 0, "e4m3 pages need 128-byte rows");
+    static_assert(!RG || (NT == 1 && !FUSE), "row groups fill one 8-column tile");
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bars[NW * STAGES];
     __shared__ int32_t stage_blk[NW * STAGES];  // physical page of each stage (-1: invalid)
@@ -726,6 +771,7 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
         ph.ctas = static_cast<int32_t>(h[2].x);
         ph.stages = static_cast<int32_t>(h[2].y);
         ph.d = static_cast<int32_t>(h[2].z);
+        ph.rg = static_cast<int32_t>(h[2].w);
         uint4* cd = reinterpret_cast<uint4*>(&cta_hdr);
 #pragma unroll
         for (int i = 0; i < 4; ++i) cd[i] = c[i];
@@ -746,14 +792,15 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
     // the pages the previous layer read last, which are still in L2.
     constexpr bool rev = REV;
     auto step = [&](Cursor& c) {
-        if (rev) retreat(p, c, cap);
-        else advance(p, c, cap);
+        if (rev) retreat<RG>(p, c, cap);
+        else advance<RG>(p, c, cap);
     };
     Cursor cc;  // page being consumed
     cc.seg_start = static_cast<int64_t>((static_cast<uint64_t>(r0.w) << 32) | r0.z);
     cc.req = static_cast<int32_t>(r1.x);
     cc.n = static_cast<int32_t>(r1.y);
-    cc.g = static_cast<int32_t>(r1.z);
+    cc.g = static_cast<int32_t>(r1.z & 0xffffu);
+    cc.nr = RG ? static_cast<int32_t>(r1.z >> 16) : 1;
     cc.pp = static_cast<int32_t>(r1.w);
     cc.kv_len = static_cast<int32_t>(r2.x);
     cc.pages = static_cast<int32_t>(r2.y);
@@ -764,7 +811,8 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
     // metadata, or none) must not steer a copy: nothing is issued, and the
     // header check below ends the launch.
     const bool rec_ok = P >= 0 && cc.req >= 0 && cc.req < p.num_reqs && cc.g >= 0 &&
-                        cc.g < p.H_kv && cc.n >= 0 && cc.n < p.max_rows && cc.pages > 0 &&
+                        cc.g < p.H_kv && cc.nr >= 1 && cc.nr <= p.rg && cc.n >= 0 &&
+                        cc.n + cc.nr <= p.max_rows && cc.pages > 0 &&
                         cc.pp >= 0 && cc.pp < cc.pages && static_cast<int64_t>(cc.pages) * BS <= cap64 + BS;
     if (!rec_ok || n_my < 0) n_my = 0;
     Cursor pc = cc;  // next page to issue (lane 0)
@@ -936,15 +984,33 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
     // 16-wide step standing for k indices {2tq, 2tq+1, 2tq+8, 2tq+9}: the query takes
     // the same order (a dot product does not depend on the order of its terms),
     // rounded to f16 to match the f16 keys.
-    auto load_q = [&](int32_t n, int32_t g) {
-        const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(p.q) +
-                                    (static_cast<int64_t>(n) * p.H_q + g * p.G) * D;
+    // Virtual head v = nt * 8 + gl of a group of nr rows is head v % G of row
+    // n + v / G (rows of one request share the walk; zero past nr * G).
+    // moff[nt][e]: how many keys fewer than the group's last row the row of
+    // accumulator column nt * 8 + 2 tq + e sees (0 past the group's rows)
+    int32_t moff[NT][2];
+    auto load_q = [&](int32_t n, int32_t g, int32_t nr) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const int h = nt * 8 + gl;
-            const bool ok = h < p.G;
+            bool ok;
+            int hr = 0, hh = 0;
+            if constexpr (RG) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+                    moff[nt][e] = nr - 1 - min((nt * 8 + 2 * tq + e) / p.G, nr - 1);
+                ok = h < nr * p.G;
+                hr = ok ? h / p.G : 0;
+                hh = ok ? h - hr * p.G : 0;
+            } else {
+                moff[nt][0] = moff[nt][1] = 0;
+                ok = h < p.G;
+                hh = ok ? h : 0;
+            }
+            const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(p.q) +
+                                        ((static_cast<int64_t>(n) + hr) * p.H_q + g * p.G + hh) * D;
             if constexpr (F8) {
-                const uint2* src = reinterpret_cast<const uint2*>(qrow + (ok ? h : 0) * D);
+                const uint2* src = reinterpret_cast<const uint2*>(qrow);
 #pragma unroll
                 for (int kk = 0; kk < S::KD; ++kk) {
                     const uint2 v = ok ? __ldg(src + kk * 4 + tq) : make_uint2(0u, 0u);
@@ -952,7 +1018,7 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
                     qf[kk][nt][1] = pack_f16x2(bf16lo_to_f32(v.y), bf16hi_to_f32(v.y));
                 }
             } else {
-                const uint32_t* src = reinterpret_cast<const uint32_t*>(qrow + (ok ? h : 0) * D);
+                const uint32_t* src = reinterpret_cast<const uint32_t*>(qrow);
 #pragma unroll
                 for (int kk = 0; kk < S::KD; ++kk) {
                     qf[kk][nt][0] = ok ? __ldg(src + kk * 8 + tq) : 0u;
@@ -988,11 +1054,11 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
     bool aborted = false;
     int consumed = 0;
     // one piece: [G][D] o, then [G] (m, l); 16-byte stride keeps float4 access aligned
-    const int piece_bytes = (p.G * (D * 4 + 8) + 15) & ~15;
+    const int piece_bytes = (p.vhs * (D * 4 + 8) + 15) & ~15;
 
     for (int i = 0; i < n_my; ++i) {
         if (i == 0 || cc.pp == (rev ? cc.pages - 1 : 0)) {
-            load_q(cc.n, cc.g);
+            load_q(cc.n, cc.g, cc.nr);
             if (fused) load_patch(cc.req, cc.g);
         }
         const int st = i % STAGES;
@@ -1138,9 +1204,27 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
             }
             // ---- online softmax ----
             // The scores stay unscaled: max(scale * s) = scale * max(s) for the positive
-            // scale, and the weights are exp2(fma(s, scale, -m)). Only a segment's last
-            // page can be partial; its keys past the causal end become -inf there.
-            if (nvalid < BS) {  // warp-uniform
+            // scale, and the weights are exp2(fma(s, scale, -m)). Only the last pages of a
+            // segment can be partial; a column's keys past its row's causal end become
+            // -inf there (the rows of a group end one key apart).
+            if constexpr (RG) {
+                const int32_t last_keys = cc.kv_len - cc.pp * BS;  // the group's last row, this page
+                if (last_keys - (cc.nr - 1) < BS) {  // warp-uniform
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const int lim0 = last_keys - moff[nt][0], lim1 = last_keys - moff[nt][1];
+#pragma unroll
+                        for (int mt = 0; mt < S::MT; ++mt) {
+                            const int t0 = mt * 16 + gl, t1 = t0 + 8;
+                            float* c = sc[mt][nt];
+                            if (t0 >= lim0) c[0] = -INFINITY;
+                            if (t0 >= lim1) c[1] = -INFINITY;
+                            if (t1 >= lim0) c[2] = -INFINITY;
+                            if (t1 >= lim1) c[3] = -INFINITY;
+                        }
+                    }
+                }
+            } else if (nvalid < BS) {  // warp-uniform
 #pragma unroll
                 for (int mt = 0; mt < S::MT; ++mt)
 #pragma unroll
@@ -1151,7 +1235,7 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
                         if (t1 >= nvalid) c[2] = c[3] = -INFINITY;
                     }
             }
-            float corr[NT][2];
+            float corr[NT][2], msafe[NT][2];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 float mx0 = -INFINITY, mx1 = -INFINITY;
@@ -1168,8 +1252,13 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
                 }
                 const float mn0 = fmaxf(m_run[nt][0], mx0 * sl2p);
                 const float mn1 = fmaxf(m_run[nt][1], mx1 * sl2p);
-                corr[nt][0] = exp2_approx(m_run[nt][0] - mn0);
-                corr[nt][1] = exp2_approx(m_run[nt][1] - mn1);
+                // a column with no key yet (a group row whose keys all lie on later
+                // pages of a backward walk) keeps m = -inf: its weights and factor
+                // are taken against 0, so that they are 0 and never NaN
+                msafe[nt][0] = (RG && mn0 == -INFINITY) ? 0.f : mn0;
+                msafe[nt][1] = (RG && mn1 == -INFINITY) ? 0.f : mn1;
+                corr[nt][0] = exp2_approx(m_run[nt][0] - msafe[nt][0]);
+                corr[nt][1] = exp2_approx(m_run[nt][1] - msafe[nt][1]);
                 m_run[nt][0] = mn0;
                 m_run[nt][1] = mn1;
             }
@@ -1196,10 +1285,10 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
                         const float* c = sc[kt][nt];
-                        const float p0 = exp2_approx(fmaf(c[0], sl2p, -m_run[nt][0]));
-                        const float p1 = exp2_approx(fmaf(c[1], sl2p, -m_run[nt][1]));
-                        const float p2 = exp2_approx(fmaf(c[2], sl2p, -m_run[nt][0]));
-                        const float p3 = exp2_approx(fmaf(c[3], sl2p, -m_run[nt][1]));
+                        const float p0 = exp2_approx(fmaf(c[0], sl2p, -msafe[nt][0]));
+                        const float p1 = exp2_approx(fmaf(c[1], sl2p, -msafe[nt][1]));
+                        const float p2 = exp2_approx(fmaf(c[2], sl2p, -msafe[nt][0]));
+                        const float p3 = exp2_approx(fmaf(c[3], sl2p, -msafe[nt][1]));
                         l_part[nt][0] += p0 + p2;
                         l_part[nt][1] += p1 + p3;
                         pb[kt][nt][0] = movmatrix_trans(pack_f16x2(p0 * vr, p1 * vr));
@@ -1247,10 +1336,10 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     const float* c = sc[kt][nt];
-                    const uint32_t lo = pack_bf16x2(exp2_approx(fmaf(c[0], sl2p, -m_run[nt][0])),
-                                                    exp2_approx(fmaf(c[1], sl2p, -m_run[nt][1])));
-                    const uint32_t hi = pack_bf16x2(exp2_approx(fmaf(c[2], sl2p, -m_run[nt][0])),
-                                                    exp2_approx(fmaf(c[3], sl2p, -m_run[nt][1])));
+                    const uint32_t lo = pack_bf16x2(exp2_approx(fmaf(c[0], sl2p, -msafe[nt][0])),
+                                                    exp2_approx(fmaf(c[1], sl2p, -msafe[nt][1])));
+                    const uint32_t hi = pack_bf16x2(exp2_approx(fmaf(c[2], sl2p, -msafe[nt][0])),
+                                                    exp2_approx(fmaf(c[3], sl2p, -msafe[nt][1])));
                     // row sums use exactly the rounded weights fed to the mma
                     l_part[nt][0] += bf16lo_to_f32(lo) + bf16lo_to_f32(hi);
                     l_part[nt][1] += bf16hi_to_f32(lo) + bf16hi_to_f32(hi);
@@ -1285,7 +1374,7 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
                     l_part[nt][1] += __shfl_xor_sync(0xffffffffu, l_part[nt][1], off);
                 }
             const int64_t s0 = cc.seg_start, s1 = cc.seg_start + cc.pages;
-            const int64_t head0 = static_cast<int64_t>(cc.n) * p.H_q + cc.g * p.G;
+            const int nvh = RG ? cc.nr * p.G : p.G;  // virtual heads of the group (row-major over its rows)
             if (s0 >= my_lo && s1 <= my_hi) {
                 // whole segment in this warp: final output
                 __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out);
@@ -1294,9 +1383,13 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int h = nt * 8 + 2 * tq + e;
-                        if (h >= p.G) continue;
+                        // a group row without any key (seq_len below its request's rows)
+                        // is zero-filled and flagged above: never written here
+                        if (h >= nvh || (RG && l_part[nt][e] == 0.f)) continue;
                         const float inv = (F8 ? vref : 1.f) / l_part[nt][e];
-                        __nv_bfloat16* dst = outp + (head0 + h) * D;
+                        const int hr = RG ? h / p.G : 0;
+                        __nv_bfloat16* dst =
+                            outp + ((static_cast<int64_t>(cc.n) + hr) * p.H_q + cc.g * p.G + (h - hr * p.G)) * D;
 #pragma unroll
                         for (int md = 0; md < S::KD; ++md) {
                             dst[drow(md, 0)] = __float2bfloat16_rn(o[md][nt][e] * inv);
@@ -1314,9 +1407,9 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
                 float2* dst_ml;
                 if (at_end) {
                     dst_o = reinterpret_cast<float*>(wbuf + slot * piece_bytes);
-                    dst_ml = reinterpret_cast<float2*>(dst_o + p.G * D);
+                    dst_ml = reinterpret_cast<float2*>(dst_o + p.vhs * D);
                 } else {
-                    const int64_t piece = (static_cast<int64_t>(wid) * 2 + slot) * p.G;
+                    const int64_t piece = (static_cast<int64_t>(wid) * 2 + slot) * p.vhs;
                     dst_o = ws.w_o + piece * D;
                     dst_ml = ws.w_ml + piece;
                 }
@@ -1325,7 +1418,7 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int h = nt * 8 + 2 * tq + e;
-                        if (h >= p.G) continue;
+                        if (h >= nvh) continue;
                         float* dst = dst_o + h * D;
                         const float of = F8 ? vref : 1.f;  // partials in true units
 #pragma unroll
@@ -1340,6 +1433,7 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
                     hdr[warp][slot].s1 = s1;
                     hdr[warp][slot].n = cc.n;
                     hdr[warp][slot].g = cc.g;
+                    hdr[warp][slot].nr = cc.nr;
                     hdr[warp][slot].o = dst_o;
                     hdr[warp][slot].ml = dst_ml;
                     hdr[warp][slot].valid = 1;
@@ -1379,19 +1473,22 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
     __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out);
     const int tph = static_cast<int>(blockDim.x) / p.G;     // threads per head (G <= 16)
     const int ch = static_cast<int>(threadIdx.x) / tph;     // this thread's head (G or more: idle)
-    const int nvec = p.G * D4;  // four-element vectors of a segment's output
+    const int VS = p.vhs;       // virtual heads per partial slot
     int e0 = 0;
     for (;;) {
         while (e0 < MAXE && !hdr[e0 >> 1][e0 & 1].valid) ++e0;
         if (e0 >= MAXE || (NT != 1 && ch >= p.G)) break;
         const int64_t s0 = hdr[e0 >> 1][e0 & 1].s0, s1 = hdr[e0 >> 1][e0 & 1].s1;
         const int32_t gn = hdr[e0 >> 1][e0 & 1].n, gg = hdr[e0 >> 1][e0 & 1].g;
+        const int32_t gnr = hdr[e0 >> 1][e0 & 1].nr;
         int e1 = e0 + 1;  // one past the group (entries in between may be invalid)
         while (e1 < MAXE && (!hdr[e1 >> 1][e1 & 1].valid || hdr[e1 >> 1][e1 & 1].s0 == s0)) ++e1;
         const bool whole = s0 >= cta_lo && s1 <= cta_hi;
         if constexpr (NT == 1) {
             const int cslot = s0 < cta_lo ? 0 : 1;
-            const int64_t head0 = static_cast<int64_t>(gn) * p.H_q + gg * p.G;
+            // groups of rows (one 8-head tile) are laid out row-major: virtual head h
+            // is head h % G of row gn + h / G
+            const int nvec = gnr * p.G * D4;  // four-element vectors of the segment's output
             for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
                 const int h = (v * 4) / D;
                 float M = -INFINITY;
@@ -1416,12 +1513,15 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
                     O.w += x.w * f;
                 }
                 if (whole) {
+                    if (RG && L == 0.f) continue;  // a group row without keys: zero-filled above
                     const float inv = 1.f / L;
-                    __nv_bfloat16* dst = outp + head0 * D + v * 4;
+                    const int hr = RG ? h / p.G : 0;
+                    __nv_bfloat16* dst = outp + ((static_cast<int64_t>(gn) + hr) * p.H_q + gg * p.G +
+                                                 (h - hr * p.G)) * D + (v * 4 - h * D);
                     reinterpret_cast<__nv_bfloat162*>(dst)[0] = __floats2bfloat162_rn(O.x * inv, O.y * inv);
                     reinterpret_cast<__nv_bfloat162*>(dst)[1] = __floats2bfloat162_rn(O.z * inv, O.w * inv);
                 } else {
-                    const int64_t cp = (static_cast<int64_t>(blockIdx.x) * 2 + cslot) * p.G + h;
+                    const int64_t cp = (static_cast<int64_t>(blockIdx.x) * 2 + cslot) * VS + h;
                     reinterpret_cast<float4*>(ws.c_o + cp * D)[(v * 4 - h * D) / 4] = O;
                     if (v * 4 - h * D == 0) ws.c_ml[cp] = make_float2(M, L);
                 }
@@ -1435,7 +1535,7 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
                 const PieceHdr& X = hdr[e >> 1][e & 1];
                 if (X.valid) M = fmaxf(M, X.ml[h].x);
             }
-            const int64_t cp = (static_cast<int64_t>(blockIdx.x) * 2 + (s0 < cta_lo ? 0 : 1)) * p.G + h;
+            const int64_t cp = (static_cast<int64_t>(blockIdx.x) * 2 + (s0 < cta_lo ? 0 : 1)) * VS + h;
             __nv_bfloat16* dsth = outp + (static_cast<int64_t>(gn) * p.H_q + gg * p.G + h) * D;
             for (int c0 = cr; c0 < D4; c0 += 4 * tph) {  // up to four vectors per pass
                 float4 O[4];
@@ -1484,7 +1584,7 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
     // can only take an SM as this grid's CTAs exit, and it waits for the whole
     // grid before it touches the workspace, queries or outputs.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    cross_cta_merge<D>(p, ws, cta_hdr, reinterpret_cast<float*>(smem));
+    cross_cta_merge<D, RG>(p, ws, cta_hdr, reinterpret_cast<float*>(smem));
 }
 
 // One-time (per device) setting of a kernel's dynamic shared memory limit.
@@ -1507,6 +1607,7 @@ cudaError_t launch_one(const CUtensorMap& mk, const CUtensorMap& mv, const AttnP
                        cudaStream_t s) {
     using S = TcShape<D, BS, F8, NT>;
     static unsigned long long smem_fwd = 0, smem_rev = 0, smem_fuse = 0;  // one per kernel
+    static unsigned long long smem_gfwd = 0, smem_grev = 0;
     const int ctas = tc_ctas(sms);
     // the cross-CTA merge keeps its tables in the (then idle) ring
     if ((16 + 2 * merge_scratch_floats(ctas, 16, D)) * 4 > S::SMEM - 1024)
@@ -1530,11 +1631,19 @@ cudaError_t launch_one(const CUtensorMap& mk, const CUtensorMap& mv, const AttnP
         e = cudaLaunchKernelEx(&cfg, attn_tc_plan<S::NW, S::STAGES, D, BS>, p);
         if (e != cudaSuccess || p.plan_only) return e;
     }
-    const bool fuse = p.k_new != nullptr;
-    auto kernel = fuse ? attn_tc_persistent<D, BS, NT, false, F8, true>
-                       : (p.reverse ? attn_tc_persistent<D, BS, NT, true, F8, false>
-                                    : attn_tc_persistent<D, BS, NT, false, F8, false>);
-    e = ensure_smem_attr(kernel, S::SMEM, fuse ? smem_fuse : (p.reverse ? smem_rev : smem_fwd));
+    const bool fuse = p.k_new != nullptr, grouped = p.rg > 1;
+    if (grouped && (NT != 1 || fuse)) return cudaErrorInvalidConfiguration;
+    // row groups: a kernel of their own (NT = 1 only)
+    constexpr bool NTG = NT == 1;
+    auto kernel = fuse ? attn_tc_persistent<D, BS, NT, false, F8, true, false>
+                  : grouped ? (p.reverse ? attn_tc_persistent<D, BS, 1, true, F8, false, NTG>
+                                         : attn_tc_persistent<D, BS, 1, false, F8, false, NTG>)
+                            : (p.reverse ? attn_tc_persistent<D, BS, NT, true, F8, false, false>
+                                         : attn_tc_persistent<D, BS, NT, false, F8, false, false>);
+    unsigned long long& done = fuse ? smem_fuse
+                               : grouped ? (p.reverse ? smem_grev : smem_gfwd)
+                                         : (p.reverse ? smem_rev : smem_fwd);
+    e = ensure_smem_attr(kernel, S::SMEM, done);
     if (e != cudaSuccess) return e;
     // With a plan made earlier and the caller's leave, the launch is a
     // programmatic dependent of the kernel before it (for example the previous

@@ -234,6 +234,16 @@ yoco_status_t run_attn(const void* q, const void* k_cache, const void* v_cache,
     p.reverse = (flags & YOCO_ATTN_REVERSE) ? 1 : 0;
     p.overlap = (flags & YOCO_ATTN_OVERLAP) ? 1 : 0;
     p.keep_tail = (flags & YOCO_ATTN_KEEP_TAIL) ? 1 : 0;
+    // Tensor-core paths: the cross rows of a request (several when max_rows
+    // exceeds num_reqs: chunked prefill, speculative verification) share one
+    // walk over the request's pages in groups that fill the kernel's 8-head
+    // tile (groups of up to 4 heads). Partial slots of grouped launches hold
+    // a full tile, those of one-row launches the G heads.
+    {
+        const int G = num_q_heads / num_kv_heads;
+        p.rg = (pl.tc && max_rows > num_reqs && G <= 4) ? 8 / G : 1;
+        p.vhs = p.rg > 1 ? 8 : G;
+    }
     p.planned = (flags & YOCO_ATTN_PLANNED) ? 1 : 0;
     p.plan_only = plan_only ? 1 : 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
