@@ -107,6 +107,16 @@ def cross_rows_kv_lens(step) -> np.ndarray:
     return np.asarray(lens, dtype=np.int64)
 
 
+def request_kv_lens(step) -> np.ndarray:
+    """Keys of the last cross row of each request with a row (its seq_len)."""
+    qsl = np.asarray(step.query_start_loc, dtype=np.int64)
+    q_len = np.diff(qsl)
+    want = np.ones_like(q_len) if step.rows_per_req is None else np.asarray(step.rows_per_req)
+    k = np.minimum(np.maximum(want, 0), np.maximum(q_len, 0))
+    seq = np.asarray(step.seq_lens, dtype=np.int64)
+    return np.maximum(seq[k > 0], 0)
+
+
 def accounting(wl, step, e4m3: bool = False) -> dict:
     """Algorithmic bytes of one step (per layer and per step). With an e4m3 cache
     the keys/values take one byte each and every page read adds its 16-byte
@@ -116,17 +126,22 @@ def accounting(wl, step, e4m3: bool = False) -> dict:
     kv_sz = 1 if e4m3 else sz
     kv = cross_rows_kv_lens(step)
     rows = int(kv.shape[0])
+    # logical bytes (the metric): every row reads its own causal prefix
     kv_bytes_layer = int(kv.sum()) * 2 * wl.num_kv_heads * wl.head_dim * kv_sz
+    # algorithmic bytes (the roofline): the rows of a request share its pages, read
+    # once up to the last row's end (seq_len keys); one row per request: the same
+    last = request_kv_lens(step)
+    uniq_kv_bytes_layer = int(last.sum()) * 2 * wl.num_kv_heads * wl.head_dim * kv_sz
     qo_bytes_layer = 2 * rows * wl.num_q_heads * wl.head_dim * sz
     page_meta = 4 + (16 if e4m3 else 0)
-    bt_bytes_layer = page_meta * int(np.sum((kv + wl.block_size - 1) // wl.block_size)) * \
+    bt_bytes_layer = page_meta * int(np.sum((last + wl.block_size - 1) // wl.block_size)) * \
         wl.num_kv_heads
     # read + write
     append_bytes = 2 * step.num_tokens * wl.num_kv_heads * wl.head_dim * (sz + kv_sz)
     return {
         "rows": rows,
         "kv_bytes_layer": kv_bytes_layer,
-        "attn_bytes_layer": kv_bytes_layer + qo_bytes_layer + bt_bytes_layer,
+        "attn_bytes_layer": uniq_kv_bytes_layer + qo_bytes_layer + bt_bytes_layer,
         "kv_bytes_step": kv_bytes_layer * wl.layers,
         "append_bytes_step": append_bytes,
         "layers": wl.layers,

@@ -202,11 +202,13 @@ size_t yoco_cross_attn_workspace_size(int32_t max_rows, int32_t num_q_heads, int
  *                          PLANNED). One workspace serves one stream at a time.
  *   err_word               device int32 or NULL
  * Several cross rows of one request (max_rows > num_reqs: chunked prefill,
- * speculative verification) with at most 4 query heads per kv head are
- * walked together on the bf16 and e4m3 paths: 8 / G consecutive rows of a
- * request share one pass over its pages (the group's last row's causal end),
- * each row masked at its own end, so the cache is read once per group, not
- * once per row. Each row's result equals its own walk up to summation order.
+ * speculative verification) with at most 8 query heads per kv head are
+ * walked together on the bf16 and e4m3 paths: consecutive rows of a request
+ * share one pass over its pages (to the group's last row's causal end), each
+ * row masked at its own end, so the cache is read once per group, not once
+ * per row. A group holds 8 / G rows when ceil(max_rows / num_reqs) rows fit
+ * in that (G <= 4), else 16 / G rows. Each row's result equals its own walk
+ * up to summation order.
  * Long contexts are split across CTAs and merged with a log-sum-exp
  * combine in a fixed split order, so results do not depend on where pages
  * sit in the pool. Accuracy: fp32 accumulation; bf16 probabilities feed the
@@ -424,12 +426,15 @@ yoco_status_t yoco_set_l2_window(void* stream, void* base, size_t bytes, float h
  * cross-decoder attention, for a traffic-aware scheduler. "YOCO 论文与推理数据流
  * 详解" §11 and §18.2: the global K^/V^ is written once but re-read by every
  * cross-decoder layer, so a request's decode traffic grows with its context
- * length times the number of cross-decoder layers. Per request r with k_r
- * cross rows (the yoco_select_cross_rows rule) and row i's key count kv_i:
- *   layers * sum_i ( kv_i * 2 * H_kv * head_dim * elem      K^ and V^
- *                  + 2 * H_q * head_dim * elem               query and output
- *                  + 4 * ceil(kv_i / block_size) * H_kv )    block-table entries
- * with elem = 2 (bf16) or 4 (fp32) and kv_i clamped at 0. For YOCO_E4M3 the
+ * length times the number of cross-decoder layers. Per request r with k_r >= 1
+ * cross rows (the yoco_select_cross_rows rule), whose last row attends to
+ * kv = seq_lens[r] keys (clamped at 0); the rows share the request's pages,
+ * which are read once:
+ *   layers * ( kv * 2 * H_kv * head_dim * elem              K^ and V^
+ *            + k_r * 2 * H_q * head_dim * elem              queries and outputs
+ *            + 4 * ceil(kv / block_size) * H_kv )           block-table entries
+ * with elem = 2 (bf16) or 4 (fp32); a request with no row moves nothing. For
+ * one row per request this is each row's own causal prefix. For YOCO_E4M3 the
  * K^/V^ term uses 1 byte per element, the query/output term 2, and each page
  * adds its 16-byte scale record next to its block-table entry.
  *   query_start_loc, seq_lens   host int32 [num_reqs + 1] / [num_reqs]

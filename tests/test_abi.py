@@ -210,9 +210,13 @@ def test_noalloc_and_l2_window_host_validation(lib_path):
                                                dt, None, None)
     assert noalloc(N.YOCO_E4M3) == N.YOCO_ERR_UNSUPPORTED
     assert noalloc(9) == N.YOCO_ERR_UNSUPPORTED
-    # a 16-wide group at head_dim 256 needs more scratch than the array holds
-    assert N.yoco_cross_attn_workspace_size(4, 16, 1, 256, 16, 4096, torch.bfloat16) > cap
-    assert noalloc(N.YOCO_BF16, H_q=16, H_kv=1) == N.YOCO_ERR_WORKSPACE
+    # the fp32 path's split grid, at the row count that makes it largest (16 heads,
+    # head_dim 256, long contexts), needs more scratch than the array holds
+    def need(r):
+        return N.yoco_cross_attn_workspace_size(r, 16, 2, 256, 16, 65536, torch.float32)
+    rows = max(range(1, 2048), key=need)
+    assert need(rows) > cap
+    assert noalloc(N.YOCO_F32, H_q=16, H_kv=2, rows=rows, ctx=65536) == N.YOCO_ERR_WORKSPACE
     L.yoco_set_l2_window.restype = ctypes.c_int
     L.yoco_set_l2_window.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
                                      ctypes.c_float]

@@ -213,7 +213,8 @@ def test_fused_step_bad_page_flagged(P, N, kv):
     assert changed.any()
 
 
-@pytest.mark.parametrize("H_q,H_kv,D,bs,draft", [(8, 2, 256, 16, 4), (4, 2, 128, 32, 3)])
+@pytest.mark.parametrize("H_q,H_kv,D,bs,draft", [(8, 2, 256, 16, 4), (4, 2, 128, 32, 3),
+                                                 (4, 4, 128, 16, 10), (16, 2, 256, 32, 2)])
 def test_e4m3_row_groups(P, H_q, H_kv, D, bs, draft):
     """Several cross rows per request over the e4m3 cache: rows grouped on one walk."""
     from workloads import spec_decode

@@ -491,12 +491,16 @@ def test_speculative_rows_small_against_oracle(P):
 
 @pytest.mark.parametrize("H_q,H_kv,D,bs,draft", [(8, 2, 256, 16, 4), (4, 4, 128, 32, 3),
                                                  (2, 2, 64, 16, 7), (3, 1, 128, 16, 5),
-                                                 (16, 1, 128, 32, 2)])
+                                                 (16, 1, 128, 32, 2), (8, 1, 128, 16, 2),
+                                                 (2, 2, 64, 32, 12), (4, 2, 256, 32, 6),
+                                                 (8, 2, 256, 16, 2)])
 def test_row_groups_against_oracle_and_page_permutation(P, H_q, H_kv, D, bs, draft):
     """Several cross rows per request (max_rows above num_reqs): rows of a request
-    share one walk over its pages in groups (groups of up to 4 heads: 8 / G rows per
-    group), each row with its own causal end. Every row of every layer against the
-    oracle, and bit-identical under a re-permutation of the physical pages."""
+    share one walk over its pages in groups whose heads fill one 8-wide tile (8 / G
+    rows, when the rows per request fit) or two (16 / G rows), each row with its own
+    causal end. The cases cover both widths, the query tile in shared memory (head_dim
+    256, two tiles) and a group of 16 one-head rows. Every row of every layer against
+    the oracle, and bit-identical under a re-permutation of the physical pages."""
     from workloads import spec_decode
     seed = 7100 + H_q * 13 + D + draft
     a = spec_decode(seed, num_reqs=5, ctx_lo=1, ctx_hi=700, draft=draft, H_q=H_q, H_kv=H_kv,

@@ -40,12 +40,19 @@ def test_model_counts_rows_like_selection(N):
     wl = chunked_prefill_spec()
     st = wl.steps[0]  # A: non-final chunk -> no row, so no bytes
     tot, per = _model(N, wl, st)
-    assert per[0] == 0 and per[1] > 0 and per[2] > per[1]
-    # three speculative rows see 201, 202, 203 keys
+    assert per[0] == 0 and per[1] > 0 and per[2] > 0
+    # three speculative rows see 201, 202, 203 keys: they share the request's pages,
+    # read once up to 203 keys, and each has its own query and output
     D, H_kv, H_q, bs, L = wl.head_dim, wl.num_kv_heads, wl.num_q_heads, wl.block_size, wl.layers
-    exp = sum(kv * 2 * H_kv * D * 2 + 2 * H_q * D * 2 + 4 * -(-kv // bs) * H_kv
-              for kv in (201, 202, 203)) * L
+    exp = (203 * 2 * H_kv * D * 2 + 3 * 2 * H_q * D * 2 + 4 * -(-203 // bs) * H_kv) * L
     assert per[2] == exp
+    # the same request with one row: only the queries and outputs of two rows fewer
+    rpr = np.asarray(st.rows_per_req).copy()
+    rpr[2] = 1
+    one, _ = N.yoco_cross_decoder_bytes(st.query_start_loc, rpr, st.seq_lens,
+                                        wl.layers, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                                        wl.block_size, torch.bfloat16)
+    assert tot - one == 2 * 2 * H_q * D * 2 * L
 
 
 def test_model_predicts_measured_dram_bytes(N):

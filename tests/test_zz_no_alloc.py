@@ -90,13 +90,17 @@ def test_noalloc_matches_workspace_entry_point(idx):
 def test_noalloc_rejects_bounds_beyond_its_array():
     N = _abi()
     cap = N.yoco_cross_attn_noalloc_capacity()
-    # bf16 with a 16-wide group at head_dim 256 needs more than the array holds
-    rows, H_q, H_kv, D, bs, ctx = 4, 16, 1, 256, 16, 4096
-    need = N.yoco_cross_attn_workspace_size(rows, H_q, H_kv, D, bs, ctx, torch.bfloat16)
+    # the fp32 path's split grid, at the row count that makes it largest (16 heads,
+    # head_dim 256, long contexts), needs more than the array holds
+    H_q, H_kv, D, bs, ctx = 16, 2, 256, 16, 65536
+    rows = max(range(1, 2048),
+               key=lambda r: N.yoco_cross_attn_workspace_size(r, H_q, H_kv, D, bs, ctx,
+                                                              torch.float32))
+    need = N.yoco_cross_attn_workspace_size(rows, H_q, H_kv, D, bs, ctx, torch.float32)
     assert need > cap
     dummy = torch.zeros(16, dtype=torch.int32, device="cuda")
     st = N.lib.yoco_cross_attn_paged_noalloc(
         dummy.data_ptr(), dummy.data_ptr(), dummy.data_ptr(), dummy.data_ptr(), dummy.data_ptr(),
         1, dummy.data_ptr(), dummy.data_ptr(), 1, rows, ctx, H_q, H_kv, D, bs, 1,
-        ctypes.c_float(0.0625), N.YOCO_BF16, None, None)
+        ctypes.c_float(0.0625), N.YOCO_F32, None, None)
     assert st == N.YOCO_ERR_WORKSPACE  # rejected before any launch

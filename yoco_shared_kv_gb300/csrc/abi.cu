@@ -119,11 +119,14 @@ extern "C" int64_t yoco_cross_decoder_bytes(const int32_t* query_start_loc,
         if (q_len < 0 || want < 0) return -1;
         const int64_t k = want < q_len ? want : q_len;
         int64_t b = 0;
-        for (int64_t i = 0; i < k; ++i) {
-            int64_t kv = static_cast<int64_t>(seq_lens[r]) - k + i + 1;
+        if (k > 0) {
+            // the rows of a request share its pages: they are read once, up to
+            // the last row's causal end (seq_len keys); each row has its own
+            // query and output
+            int64_t kv = seq_lens[r];
             if (kv < 0) kv = 0;
-            b += kv * 2 * num_kv_heads * head_dim * kv_elem + 2ll * num_q_heads * head_dim * elem +
-                 page_meta * ((kv + block_size - 1) / block_size) * num_kv_heads;
+            b = kv * 2 * num_kv_heads * head_dim * kv_elem + k * 2ll * num_q_heads * head_dim * elem +
+                page_meta * ((kv + block_size - 1) / block_size) * num_kv_heads;
         }
         b *= layers;
         if (per_req_bytes) per_req_bytes[r] = b;

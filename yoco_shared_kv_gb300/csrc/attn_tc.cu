@@ -24,13 +24,21 @@ int tc_ctas(int sms) { return sms < kMaxCtas ? sms : kMaxCtas; }
 size_t tc_workspace_bytes(int sms, int H_kv, int G, int D, int BS, bool e4m3) {
     (void)H_kv;
     const int64_t ctas = tc_ctas(sms);
-    const bool wide = G > 8;  // two 8-head tiles
-    const int nw = e4m3 ? (wide ? nw_of<true, 2>(D, BS) : nw_of<true, 1>(D, BS))
-                        : (wide ? nw_of<false, 2>(D, BS) : nw_of<false, 1>(D, BS));
-    // a partial slot holds the G heads of one row, or the 8 virtual heads of a
-    // group of rows sharing one walk: max(G, 8) covers both
-    const size_t pieces = static_cast<size_t>(tc_pieces(ctas, nw, G > 8 ? G : 8));
-    return static_cast<size_t>(tc_plan_bytes(ctas, nw)) + pieces * (static_cast<size_t>(D) * 4 + 8);
+    auto need = [&](int nw, int vs) {
+        return static_cast<size_t>(tc_plan_bytes(ctas, nw)) +
+               static_cast<size_t>(tc_pieces(ctas, nw, vs)) * (static_cast<size_t>(D) * 4 + 8);
+    };
+    // Two 8-head tiles (NT = 2) run for groups wider than 8 and for cross rows
+    // grouped 16 virtual heads wide; one tile for the rest (8 virtual heads at
+    // most). A partial slot holds one tile's heads.
+    const int nw2 = e4m3 ? nw_of<true, 2>(D, BS) : nw_of<false, 2>(D, BS);
+    size_t b = need(nw2, 16);
+    if (G <= 8) {
+        const int nw1 = e4m3 ? nw_of<true, 1>(D, BS) : nw_of<false, 1>(D, BS);
+        const size_t b1 = need(nw1, 8);
+        if (b1 > b) b = b1;
+    }
+    return b;
 }
 
 cudaError_t launch_attn_tc(const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p,

@@ -90,8 +90,15 @@ struct TcShape {
     static constexpr int SUB_BYTES = BS * 128;
     static constexpr int MT = BS / 16;   // 16-token tiles per page
     static constexpr int KD = D / 16;    // 16-wide steps along head_dim
-    static constexpr int SMEM = NW * STAGES * STAGE_BYTES + 1024;
-    static_assert(SMEM <= 200 * 1024, "the rings must leave room for static shared memory");
+    // Two 8-head tiles at head_dim 256 would hold the queries in 64 registers
+    // on top of the 128 of the output accumulators: there the queries of the
+    // segment sit in shared memory instead (16 rows x D, 16-bit), read per
+    // page with ldmatrix.
+    static constexpr bool QSM = D == 256 && NT == 2;
+    static constexpr int Q_BYTES = QSM ? 16 * D * 2 : 0;  // per warp
+    static constexpr int RING_BYTES = NW * STAGES * STAGE_BYTES;
+    static constexpr int SMEM = RING_BYTES + NW * Q_BYTES + 1024;
+    static_assert(SMEM <= 225 * 1024, "the rings must leave room for static shared memory");
 };
 
 // Byte offset of (token t, 16-byte chunk j of head-dim sub-tile c) in a
@@ -320,8 +327,10 @@ static_assert(sizeof(CtaHdr) == 64, "CTA header size");
 // Workspace carve-up (every part a multiple of 16 bytes):
 //   plan header, forward and reverse WarpPlan records [2][C][NW], CtaHdr [C],
 //   arrival counters [C] (one per CTA, used by the segment starting in it),
-//   [W + C][2][G][D] partial outputs (warp pieces, then CTA pieces),
-//   [W + C][2][G] (m, l).
+//   partial outputs: [W][VS][D] (each warp's one mid-slice piece), then
+//   [C][2][VS][D] (each CTA's first / last segment), and their (m, l) in the
+//   same order, VS = p.vhs virtual heads per slot. A warp's slice-end piece
+//   stays in its ring.
 struct TcWs {
     PlanHdr* plan;
     WarpPlan* wplan;  // [2][C * NW]: forward walks, then reverse walks
@@ -333,8 +342,8 @@ struct TcWs {
     float2* c_ml;
 };
 
-__host__ __device__ __forceinline__ int64_t tc_pieces(int64_t ctas, int nw, int G) {
-    return (ctas * nw + ctas) * 2 * G;
+__host__ __device__ __forceinline__ int64_t tc_pieces(int64_t ctas, int nw, int VS) {
+    return (ctas * nw + 2 * ctas) * VS;
 }
 
 __host__ __device__ __forceinline__ int64_t tc_plan_bytes(int64_t ctas, int nw) {
@@ -351,12 +360,11 @@ __device__ __forceinline__ TcWs tc_ws(const AttnParams& p, int ctas, int nw, int
     w.hdr = reinterpret_cast<CtaHdr*>(w.wplan + 2ll * ctas * nw);
     w.cnt = reinterpret_cast<uint32_t*>(w.hdr + ctas);
     float* o = reinterpret_cast<float*>(base + tc_plan_bytes(ctas, nw));
-    const int64_t per = 2ll * p.vhs;  // pieces per worker (first / last segment) x virtual heads
     const int64_t W = static_cast<int64_t>(ctas) * nw;
     w.w_o = o;
-    w.c_o = o + W * per * D;
+    w.c_o = o + W * p.vhs * D;
     w.w_ml = reinterpret_cast<float2*>(o + tc_pieces(ctas, nw, p.vhs) * D);
-    w.c_ml = w.w_ml + W * per;
+    w.c_ml = w.w_ml + W * p.vhs;
     return w;
 }
 
@@ -699,7 +707,7 @@ __device__ __forceinline__ void cross_cta_merge(const AttnParams& p, const TcWs&
 
 // FUSE: fused decode step (append this step's tokens, patch them into the
 // copied pages); instantiated with REV = false only.
-// RG: cross rows grouped on one walk (p.rg > 1; NT = 1 and FUSE = false only).
+// RG: cross rows grouped on one walk (p.rg > 1; FUSE = false only).
 // Without it every segment is one row and the per-column causal masks and
 // the guard for columns without keys compile away.
 template <int D, int BS, int NT, bool REV, bool F8, bool FUSE, bool RG>
@@ -711,7 +719,7 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
     static_assert(S::PIECE_PAIR <= STAGES * S::STAGE_BYTES,
                   "a warp's two end-of-slice pieces must fit in its ring");
     static_assert(!F8 || D % 128 == 0, "e4m3 pages need 128-byte rows");
-    static_assert(!RG || (NT == 1 && !FUSE), "row groups fill one 8-column tile");
+    static_assert(!RG || !FUSE, "the fused decode step has one row per request");
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bars[NW * STAGES];
     __shared__ int32_t stage_blk[NW * STAGES];  // physical page of each stage (-1: invalid)
@@ -958,7 +966,7 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
             }
         }
     }
-    uint32_t qf[S::KD][NT][2];
+    uint32_t qf[S::QSM ? 1 : S::KD][NT][2];  // queries in registers (not with QSM)
     float o[S::KD][NT][4];
     float m_run[NT][2], l_part[NT][2];
     // e4m3: o holds sum p * (v_scale / vref) * code; vref is the V scale of the
@@ -989,40 +997,106 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
     // moff[nt][e]: how many keys fewer than the group's last row the row of
     // accumulator column nt * 8 + 2 tq + e sees (0 past the group's rows)
     int32_t moff[NT][2];
+    // QSM: the segment's queries as 16 rows (virtual heads) of D 16-bit values
+    // in this warp's own shared-memory tile, 16-byte chunk j of row h at
+    // h * 2D + ((j ^ (h & 7)) << 4) so that the 8 rows an ldmatrix reads fall
+    // in distinct banks. For e4m3 keys each 16-dim step holds the f16 query in
+    // the keys' order: chunk 2kk dims {0,1,4,5,8,9,12,13}, chunk 2kk + 1 dims
+    // {2,3,6,7,10,11,14,15} (of step kk), so that a lane's ldmatrix pairs are
+    // the dims its key registers hold.
+    uint8_t* const qsm = smem + S::RING_BYTES + warp * S::Q_BYTES;
+    auto load_q_smem = [&](int32_t n, int32_t g, int32_t nr) {
+        const int nvh = RG ? nr * p.G : p.G;
+        auto qsrc = [&](int h) {
+            const int hr = RG ? h / p.G : 0, hh = h - hr * p.G;
+            return static_cast<const __nv_bfloat16*>(p.q) +
+                   ((static_cast<int64_t>(n) + hr) * p.H_q + g * p.G + hh) * D;
+        };
+        __syncwarp();  // the previous segment's ldmatrix reads are done
+        if constexpr (F8) {
+            constexpr int NB = D / 16;  // 16-dim steps per row
+            static_assert(32 % NB == 0, "whole rows per pass");
+#pragma unroll 1
+            for (int x = lane; x < 16 * NB; x += 32) {
+                const int h = x / NB, kk = x - h * NB;
+                uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
+                if (h < nvh) {
+                    const uint4* src = reinterpret_cast<const uint4*>(qsrc(h) + kk * 16);
+                    a = __ldg(src);
+                    b = __ldg(src + 1);
+                }
+                auto w = [](uint32_t v) { return pack_f16x2(bf16lo_to_f32(v), bf16hi_to_f32(v)); };
+                uint8_t* row = qsm + h * (2 * D);
+                *reinterpret_cast<uint4*>(row + (((2 * kk) ^ (h & 7)) << 4)) =
+                    make_uint4(w(a.x), w(a.z), w(b.x), w(b.z));
+                *reinterpret_cast<uint4*>(row + (((2 * kk + 1) ^ (h & 7)) << 4)) =
+                    make_uint4(w(a.y), w(a.w), w(b.y), w(b.w));
+            }
+        } else {
+            constexpr int NCH = D / 8;  // 16-byte chunks per row
+            static_assert(32 % NCH == 0 || NCH % 32 == 0, "whole rows per pass");
+#pragma unroll 1
+            for (int x = lane; x < 16 * NCH; x += 32) {
+                const int h = x / NCH, j = x - h * NCH;
+                const uint4 v = h < nvh ? __ldg(reinterpret_cast<const uint4*>(qsrc(h)) + j)
+                                        : make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(qsm + h * (2 * D) + ((j ^ (h & 7)) << 4)) = v;
+            }
+        }
+        __syncwarp();
+    };
+    // this lane's ldmatrix row of the query tile: matrices (rows 0-7 | 8-15) x
+    // (chunk 2kk | 2kk + 1), so the four registers are n-tile 0's b0, b1, then
+    // n-tile 1's
+    const uint32_t q_lane = smem_u32(qsm) + (((lane >> 4) * 8 + (lane & 7)) * (2 * D));
+    auto q_addr = [&](int kk) {
+        return q_lane + ((((2 * kk) + ((lane >> 3) & 1)) ^ (lane & 7)) << 4);
+    };
     auto load_q = [&](int32_t n, int32_t g, int32_t nr) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const int h = nt * 8 + gl;
-            bool ok;
-            int hr = 0, hh = 0;
+        if constexpr (S::QSM) {
             if constexpr (RG) {
 #pragma unroll
-                for (int e = 0; e < 2; ++e)
-                    moff[nt][e] = nr - 1 - min((nt * 8 + 2 * tq + e) / p.G, nr - 1);
-                ok = h < nr * p.G;
-                hr = ok ? h / p.G : 0;
-                hh = ok ? h - hr * p.G : 0;
-            } else {
-                moff[nt][0] = moff[nt][1] = 0;
-                ok = h < p.G;
-                hh = ok ? h : 0;
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e)
+                        moff[nt][e] = nr - 1 - min((nt * 8 + 2 * tq + e) / p.G, nr - 1);
             }
-            const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(p.q) +
-                                        ((static_cast<int64_t>(n) + hr) * p.H_q + g * p.G + hh) * D;
-            if constexpr (F8) {
-                const uint2* src = reinterpret_cast<const uint2*>(qrow);
+            load_q_smem(n, g, nr);
+        } else {
 #pragma unroll
-                for (int kk = 0; kk < S::KD; ++kk) {
-                    const uint2 v = ok ? __ldg(src + kk * 4 + tq) : make_uint2(0u, 0u);
-                    qf[kk][nt][0] = pack_f16x2(bf16lo_to_f32(v.x), bf16hi_to_f32(v.x));
-                    qf[kk][nt][1] = pack_f16x2(bf16lo_to_f32(v.y), bf16hi_to_f32(v.y));
+            for (int nt = 0; nt < NT; ++nt) {
+                const int h = nt * 8 + gl;
+                bool ok;
+                int hr = 0, hh = 0;
+                if constexpr (RG) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e)
+                        moff[nt][e] = nr - 1 - min((nt * 8 + 2 * tq + e) / p.G, nr - 1);
+                    ok = h < nr * p.G;
+                    hr = ok ? h / p.G : 0;
+                    hh = ok ? h - hr * p.G : 0;
+                } else {
+                    moff[nt][0] = moff[nt][1] = 0;
+                    ok = h < p.G;
+                    hh = ok ? h : 0;
                 }
-            } else {
-                const uint32_t* src = reinterpret_cast<const uint32_t*>(qrow);
+                const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(p.q) +
+                                            ((static_cast<int64_t>(n) + hr) * p.H_q + g * p.G + hh) * D;
+                if constexpr (F8) {
+                    const uint2* src = reinterpret_cast<const uint2*>(qrow);
 #pragma unroll
-                for (int kk = 0; kk < S::KD; ++kk) {
-                    qf[kk][nt][0] = ok ? __ldg(src + kk * 8 + tq) : 0u;
-                    qf[kk][nt][1] = ok ? __ldg(src + kk * 8 + 4 + tq) : 0u;
+                    for (int kk = 0; kk < S::KD; ++kk) {
+                        const uint2 v = ok ? __ldg(src + kk * 4 + tq) : make_uint2(0u, 0u);
+                        qf[kk][nt][0] = pack_f16x2(bf16lo_to_f32(v.x), bf16hi_to_f32(v.x));
+                        qf[kk][nt][1] = pack_f16x2(bf16lo_to_f32(v.y), bf16hi_to_f32(v.y));
+                    }
+                } else {
+                    const uint32_t* src = reinterpret_cast<const uint32_t*>(qrow);
+#pragma unroll
+                    for (int kk = 0; kk < S::KD; ++kk) {
+                        qf[kk][nt][0] = ok ? __ldg(src + kk * 8 + tq) : 0u;
+                        qf[kk][nt][1] = ok ? __ldg(src + kk * 8 + 4 + tq) : 0u;
+                    }
                 }
             }
         }
@@ -1146,7 +1220,58 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
 #pragma unroll
                         for (int c = 0; c < 4; ++c) sc[mt][nt][c] = sc2[mt][nt][c] = 0.f;
                 const int mi = lane >> 3, rr = lane & 7;
-                if constexpr (F8) {
+                if constexpr (S::QSM && F8) {
+                    // as below, with the query fragments read from the warp's tile
+                    // once per pair of k steps for all token tiles
+#pragma unroll
+                    for (int kp = 0; kp < S::KD / 2; ++kp) {
+                        uint32_t qa[4], qb[4];
+                        ldsm_x4(q_addr(2 * kp), qa[0], qa[1], qa[2], qa[3]);
+                        ldsm_x4(q_addr(2 * kp + 1), qb[0], qb[1], qb[2], qb[3]);
+#pragma unroll
+                        for (int mt = 0; mt < S::MT; ++mt) {
+                            const int t = mt * 16 + (mi & 1) * 8 + rr;
+                            const int ch = 2 * kp + (mi >> 1);
+                            uint32_t r0, r1, r2, r3;
+                            ldsm_x4(kbase + swz<BS>(ch >> 3, t, ch & 7), r0, r1, r2, r3);
+                            const uint32_t a0 = e4m3x2_lo_to_f16x2(r0);
+                            const uint32_t a1 = e4m3x2_lo_to_f16x2(r1);
+                            const uint32_t a2 = e4m3x2_hi_to_f16x2(r0);
+                            const uint32_t a3 = e4m3x2_hi_to_f16x2(r1);
+                            const uint32_t b0 = e4m3x2_lo_to_f16x2(r2);
+                            const uint32_t b1 = e4m3x2_lo_to_f16x2(r3);
+                            const uint32_t b2 = e4m3x2_hi_to_f16x2(r2);
+                            const uint32_t b3 = e4m3x2_hi_to_f16x2(r3);
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt) {
+                                mma_f16_16816(sc[mt][nt], a0, a1, a2, a3, qa[2 * nt], qa[2 * nt + 1]);
+                                mma_f16_16816(sc2[mt][nt], b0, b1, b2, b3, qb[2 * nt], qb[2 * nt + 1]);
+                            }
+                        }
+                    }
+                } else if constexpr (S::QSM) {
+#pragma unroll
+                    for (int kk = 0; kk < S::KD; ++kk) {
+                        uint32_t qk[4];
+                        ldsm_x4(q_addr(kk), qk[0], qk[1], qk[2], qk[3]);
+#pragma unroll
+                        for (int mt = 0; mt < S::MT; ++mt) {
+                            const int t = mt * 16 + (mi & 1) * 8 + rr;
+                            uint32_t a0, a1, a2, a3;
+                            ldsm_x4(kbase + swz<BS>(kk >> 2, t, (kk & 3) * 2 + (mi >> 1)), a0, a1,
+                                    a2, a3);
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt) {
+                                if (kk & 1)
+                                    mma_bf16_16816(sc2[mt][nt], a0, a1, a2, a3, qk[2 * nt],
+                                                   qk[2 * nt + 1]);
+                                else
+                                    mma_bf16_16816(sc[mt][nt], a0, a1, a2, a3, qk[2 * nt],
+                                                   qk[2 * nt + 1]);
+                            }
+                        }
+                    }
+                } else if constexpr (F8) {
                     // one ldmatrix.x4 = 16 tokens x 32 head dims (two k steps); a lane's
                     // 32-bit register holds 4 consecutive e4m3 of one token
 #pragma unroll
@@ -1400,8 +1525,9 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
                 const int slot = s0 < my_lo ? 0 : 1;
                 // A piece flushed at the end of the slice goes to this warp's
                 // ring, idle from here on; the one flushed mid-stream (the
-                // first segment walked) goes to the workspace, where the
-                // combine reads it.
+                // first segment walked: it began before the slice and ends
+                // inside it, so its slot is 0) goes to the workspace, where
+                // the combine reads it.
                 const bool at_end = (i == n_my - 1);
                 float* dst_o;
                 float2* dst_ml;
@@ -1409,7 +1535,7 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
                     dst_o = reinterpret_cast<float*>(wbuf + slot * piece_bytes);
                     dst_ml = reinterpret_cast<float2*>(dst_o + p.vhs * D);
                 } else {
-                    const int64_t piece = (static_cast<int64_t>(wid) * 2 + slot) * p.vhs;
+                    const int64_t piece = static_cast<int64_t>(wid) * p.vhs;
                     dst_o = ws.w_o + piece * D;
                     dst_ml = ws.w_ml + piece;
                 }
@@ -1471,18 +1597,24 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
     constexpr int MAXE = 2 * NW;
     constexpr int D4 = D / 4;  // four-element vectors per head
     __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out);
-    const int tph = static_cast<int>(blockDim.x) / p.G;     // threads per head (G <= 16)
-    const int ch = static_cast<int>(threadIdx.x) / tph;     // this thread's head (G or more: idle)
     const int VS = p.vhs;       // virtual heads per partial slot
+    // two tiles: threads per (virtual) head, and this thread's head (past the
+    // segment's heads: idle)
+    const int tph = static_cast<int>(blockDim.x) / (RG ? VS : p.G);
+    const int ch = static_cast<int>(threadIdx.x) / tph;
     int e0 = 0;
     for (;;) {
         while (e0 < MAXE && !hdr[e0 >> 1][e0 & 1].valid) ++e0;
-        if (e0 >= MAXE || (NT != 1 && ch >= p.G)) break;
+        if (e0 >= MAXE || (NT != 1 && !RG && ch >= p.G)) break;
         const int64_t s0 = hdr[e0 >> 1][e0 & 1].s0, s1 = hdr[e0 >> 1][e0 & 1].s1;
         const int32_t gn = hdr[e0 >> 1][e0 & 1].n, gg = hdr[e0 >> 1][e0 & 1].g;
         const int32_t gnr = hdr[e0 >> 1][e0 & 1].nr;
         int e1 = e0 + 1;  // one past the group (entries in between may be invalid)
         while (e1 < MAXE && (!hdr[e1 >> 1][e1 & 1].valid || hdr[e1 >> 1][e1 & 1].s0 == s0)) ++e1;
+        if (NT != 1 && RG && ch >= gnr * p.G) {  // no head of this thread in the group
+            e0 = e1;
+            continue;
+        }
         const bool whole = s0 >= cta_lo && s1 <= cta_hi;
         if constexpr (NT == 1) {
             const int cslot = s0 < cta_lo ? 0 : 1;
@@ -1536,7 +1668,9 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
                 if (X.valid) M = fmaxf(M, X.ml[h].x);
             }
             const int64_t cp = (static_cast<int64_t>(blockIdx.x) * 2 + (s0 < cta_lo ? 0 : 1)) * VS + h;
-            __nv_bfloat16* dsth = outp + (static_cast<int64_t>(gn) * p.H_q + gg * p.G + h) * D;
+            const int hr = RG ? h / p.G : 0;  // virtual head h: head h % G of row gn + h / G
+            __nv_bfloat16* dsth =
+                outp + ((static_cast<int64_t>(gn) + hr) * p.H_q + gg * p.G + (h - hr * p.G)) * D;
             for (int c0 = cr; c0 < D4; c0 += 4 * tph) {  // up to four vectors per pass
                 float4 O[4];
 #pragma unroll
@@ -1567,6 +1701,7 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
                     const int j = c0 + u * tph;
                     if (j >= D4) continue;
                     if (whole) {
+                        if (RG && L == 0.f) continue;  // a group row without keys: zero-filled above
                         __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(dsth + j * 4);
                         dst[0] = __floats2bfloat162_rn(O[u].x * inv, O[u].y * inv);
                         dst[1] = __floats2bfloat162_rn(O[u].z * inv, O[u].w * inv);
@@ -1632,12 +1767,11 @@ cudaError_t launch_one(const CUtensorMap& mk, const CUtensorMap& mv, const AttnP
         if (e != cudaSuccess || p.plan_only) return e;
     }
     const bool fuse = p.k_new != nullptr, grouped = p.rg > 1;
-    if (grouped && (NT != 1 || fuse)) return cudaErrorInvalidConfiguration;
-    // row groups: a kernel of their own (NT = 1 only)
-    constexpr bool NTG = NT == 1;
+    if (grouped && fuse) return cudaErrorInvalidConfiguration;
+    // row groups: kernels of their own
     auto kernel = fuse ? attn_tc_persistent<D, BS, NT, false, F8, true, false>
-                  : grouped ? (p.reverse ? attn_tc_persistent<D, BS, 1, true, F8, false, NTG>
-                                         : attn_tc_persistent<D, BS, 1, false, F8, false, NTG>)
+                  : grouped ? (p.reverse ? attn_tc_persistent<D, BS, NT, true, F8, false, true>
+                                         : attn_tc_persistent<D, BS, NT, false, F8, false, true>)
                             : (p.reverse ? attn_tc_persistent<D, BS, NT, true, F8, false, false>
                                          : attn_tc_persistent<D, BS, NT, false, F8, false, false>);
     unsigned long long& done = fuse ? smem_fuse
@@ -1658,7 +1792,7 @@ cudaError_t launch_one(const CUtensorMap& mk, const CUtensorMap& mv, const AttnP
 template <int D, bool F8>
 cudaError_t launch_d(const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p, int BS,
                      int sms, cudaStream_t s) {
-    const bool wide = p.G > 8;
+    const bool wide = p.vhs > 8;  // two 8-head tiles: a group over 8, or 16 virtual heads
     if (BS == 16) return wide ? launch_one<D, 16, 2, F8>(mk, mv, p, sms, s)
                               : launch_one<D, 16, 1, F8>(mk, mv, p, sms, s);
     return wide ? launch_one<D, 32, 2, F8>(mk, mv, p, sms, s)

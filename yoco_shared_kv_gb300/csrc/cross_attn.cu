@@ -236,13 +236,25 @@ yoco_status_t run_attn(const void* q, const void* k_cache, const void* v_cache,
     p.keep_tail = (flags & YOCO_ATTN_KEEP_TAIL) ? 1 : 0;
     // Tensor-core paths: the cross rows of a request (several when max_rows
     // exceeds num_reqs: chunked prefill, speculative verification) share one
-    // walk over the request's pages in groups that fill the kernel's 8-head
-    // tile (groups of up to 4 heads). Partial slots of grouped launches hold
-    // a full tile, those of one-row launches the G heads.
+    // walk over the request's pages in groups of rows whose heads fill the
+    // kernel's head tile: one 8-wide tile when the rows per request (bounded
+    // by max_rows / num_reqs) fit in it, else two (16 virtual heads). Partial
+    // slots of grouped launches hold a full tile, those of one-row launches
+    // the G heads; NT = 2 tiles run when the slot is wider than 8.
     {
         const int G = num_q_heads / num_kv_heads;
-        p.rg = (pl.tc && max_rows > num_reqs && G <= 4) ? 8 / G : 1;
-        p.vhs = p.rg > 1 ? 8 : G;
+        const int64_t per_req = (static_cast<int64_t>(max_rows) + num_reqs - 1) / num_reqs;
+        p.rg = 1;
+        p.vhs = G;
+        if (pl.tc && per_req > 1 && G <= 8) {
+            if (G <= 4 && per_req <= 8 / G) {
+                p.rg = 8 / G;
+                p.vhs = 8;
+            } else {
+                p.rg = 16 / G;
+                p.vhs = 16;
+            }
+        }
     }
     p.planned = (flags & YOCO_ATTN_PLANNED) ? 1 : 0;
     p.plan_only = plan_only ? 1 : 0;
