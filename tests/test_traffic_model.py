@@ -58,13 +58,15 @@ def test_model_counts_rows_like_selection(N):
 def test_model_predicts_measured_dram_bytes(N):
     """profiles/traffic.txt holds ncu DRAM bytes per attention launch at full size; a launch
     measured alone (caches flushed, no reuse between layers) reads what the model predicts
-    (its writes add the workspace partials of the cross-CTA merge, ~1% of the bytes)."""
+    (its writes add the workspace partials of the cross-CTA merge, ~1% of the bytes),
+    including the speculative workload, whose rows share their request's pages."""
     import bench
     lines = open(os.path.join(ROOT, "profiles", "traffic.txt")).read().splitlines()
     meas = dict(l.split("=", 1) for l in lines if "=" in l and not l.startswith("#"))
+    # 5: four rows per request, grouped on one walk: the request's pages are read once
     for cfg, name, e4m3 in ((1, "pure_decode_bf16", False), (3, "long_context_bf16", False),
                             (1, "pure_decode_bf16_e4m3kv", True),
-                            (3, "long_context_bf16_e4m3kv", True)):
+                            (3, "long_context_bf16_e4m3kv", True), (5, "spec_decode_bf16", False)):
         wl = bench.make_workload(cfg)
         st = wl.steps[-1]
         dt = torch.float8_e4m3fn if e4m3 else torch.bfloat16
