@@ -576,3 +576,42 @@ def test_row_group_with_an_empty_row(P, N):
     st = dataclasses.replace(wl.steps[0], seq_lens=sl.cpu().numpy())
     ref = oracle_step_out(wl, st, layers=[0], rows=[r for r in range(12) if r != 4])[0]
     assert np.abs(np.delete(got, 4, axis=0) - ref).max() <= ATOL["bf16"]
+
+
+@pytest.mark.parametrize("kv", ["native", "e4m3"])
+def test_loose_max_rows_over_one_row_requests(P, N, kv):
+    """max_rows well above the rows the selection produced (a caller's loose bound): the
+    launch then takes the 16-wide row-group kernel (max_rows / num_reqs = 4 rows per
+    request at four heads per kv head) although every request has one row. The real rows
+    match the oracle; rows past them are neither read nor written."""
+    from workloads import page_scales
+    wl = pure_decode(7600, num_reqs=6, ctx_lo=1, ctx_hi=800, layers=1)
+    e4m3 = kv == "e4m3"
+    dw = P.DeviceWorkload(wl, kv="e4m3", page_scales=page_scales(wl)) if e4m3 \
+        else P.DeviceWorkload(wl)
+    dw.run_all()
+    torch.cuda.synchronize()
+    assert dw.error_bits() == 0
+    ds = dw.steps[0]
+    R = ds.out.shape[1]
+    cap = 4 * R
+    q = torch.full((cap, wl.num_q_heads, wl.head_dim), float("nan"), dtype=torch.bfloat16,
+                   device="cuda")
+    q[:R] = ds.dev["q"][0]
+    out = torch.full_like(q, 7.0)
+    if e4m3:
+        N.yoco_cross_attn_paged_e4m3(q, dw.k_cache, dw.v_cache, dw.page_scales, out,
+                                     ds.dev["block_table"], ds.dev["seq_lens"], ds.cqsl,
+                                     ds.max_seq_len, wl.scale, ds.workspace, dw.err)
+    else:
+        N.yoco_cross_attn_paged(q, dw.k_cache, dw.v_cache, out, ds.dev["block_table"],
+                                ds.dev["seq_lens"], ds.cqsl, ds.max_seq_len, wl.scale,
+                                ds.workspace, dw.err)
+    torch.cuda.synchronize()
+    assert dw.error_bits() == 0
+    assert (out[R:] == 7.0).all()
+    # the same rows as the step's own (exact max_rows) launch, and the oracle's
+    assert np.abs(gpu_out(out[:R]) - gpu_out(ds.out[0])).max() <= ATOL["bf16"]
+    if not e4m3:
+        ref = oracle_step_out(wl, wl.steps[0])[0]
+        assert np.abs(gpu_out(out[:R]) - ref).max() <= ATOL["bf16"]
