@@ -216,11 +216,12 @@ def test_fused_step_bad_page_flagged(P, N, kv):
 @pytest.mark.parametrize("H_q,H_kv,D,bs,draft", [(8, 2, 256, 16, 4), (4, 2, 128, 32, 3),
                                                  (4, 4, 128, 16, 10), (16, 2, 256, 32, 2)])
 def test_e4m3_row_groups(P, H_q, H_kv, D, bs, draft):
-    """Several cross rows per request over the e4m3 cache: rows grouped on one walk."""
+    """Several cross rows per request over the e4m3 cache: rows grouped on one walk
+    (8- and 16-wide groups; the second layer walks its pages backwards)."""
     from workloads import spec_decode
     wl = spec_decode(7400 + H_q + draft, num_reqs=5, ctx_lo=1, ctx_hi=700, draft=draft, H_q=H_q,
                      H_kv=H_kv, D=D, bs=bs, layers=2)
     scales = page_scales(wl)
-    dw = _run(P, wl, scales)
+    dw = _run(P, wl, scales, alternate=True)
     assert dw.error_bits() == 0
     _check_steps(wl, dw, scales, layers=[0, 1])

@@ -6,7 +6,7 @@ import torch
 
 from tests.helpers import (ATOL, gpu_out, oracle_e4m3_pools, oracle_e4m3_step_out, oracle_pools,
                            oracle_step_out, pool_bits, oracle_bits)
-from workloads import SMALL, page_scales
+from workloads import SMALL, page_scales, pure_decode
 
 pytestmark = pytest.mark.gpu
 
@@ -32,10 +32,17 @@ def _pair(P, wl, kv):
     return a, b, sc
 
 
+def _wide_decode():
+    # 16 query heads per kv head at head_dim 256: two 8-head tiles, the queries in the
+    # warp's shared-memory tile
+    return pure_decode(8100, num_reqs=5, ctx_lo=1, ctx_hi=600, H_q=32, H_kv=2, D=256, bs=16,
+                       layers=2)
+
+
 @pytest.mark.parametrize("kv", ["native", "e4m3"])
-@pytest.mark.parametrize("idx", [1, 4])
+@pytest.mark.parametrize("idx", [1, 4, "wide"])
 def test_fused_step_equals_separate_calls(P, idx, kv):
-    wl = SMALL[idx]()
+    wl = _wide_decode() if idx == "wide" else SMALL[idx]()
     a, b, sc = _pair(P, wl, kv)
     for dw in (a, b):
         dw.run_fill()
