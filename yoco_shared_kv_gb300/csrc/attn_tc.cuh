@@ -47,12 +47,15 @@ namespace yoco {
 namespace {
 
 // Warps per CTA and ring depth per warp for 16 KiB stages (compile-time
-// tunables; the defaults fill about 192 KiB of shared memory).
+// tunables; the defaults fill 192 KiB of shared memory). Six warps of two
+// stages keep as many bytes in flight as four of three, with half again as
+// many warps to hide each page's chain of dependent steps. The warp count
+// must be even.
 #ifndef YOCO_TC_NW16
-#define YOCO_TC_NW16 4
+#define YOCO_TC_NW16 6
 #endif
 #ifndef YOCO_TC_ST16
-#define YOCO_TC_ST16 3
+#define YOCO_TC_ST16 2
 #endif
 // e4m3 cache: warps per CTA and shared-memory bytes of the warps' rings
 // (0 = derived from the piece sizes, below)
@@ -79,12 +82,17 @@ struct TcShape {
         PIECE_PAIR <= YOCO_TC_F8_RING / 4 && 2 * STAGE_BYTES <= YOCO_TC_F8_RING / 4;
     static constexpr int F8_NW =
         YOCO_TC_F8_NW > 0 ? YOCO_TC_F8_NW : (F8_FITS8 ? 8 : (F8_FITS4 ? 4 : 2));
+    // Two 8-head tiles at head_dim 256 hold the queries in shared memory (below):
+    // their kernels keep 4 warps x 3 stages whatever the tunables say.
+    static constexpr bool QSM = D == 256 && NT == 2;
     static constexpr int NW =
-        F8 ? F8_NW : (STAGE_BYTES <= 8192 ? 8 : (STAGE_BYTES <= 16384 ? YOCO_TC_NW16 : 2));
+        F8 ? F8_NW
+           : (STAGE_BYTES <= 8192 ? 8 : (STAGE_BYTES <= 16384 ? (QSM ? 4 : YOCO_TC_NW16) : 2));
     // e4m3 pages are small: deepen the ring to keep ~192 KiB in flight per SM
     static constexpr int F8_STAGES = YOCO_TC_F8_RING / F8_NW / STAGE_BYTES;
     static constexpr int STAGES =
-        F8 ? (F8_STAGES < 2 ? 2 : F8_STAGES) : (STAGE_BYTES == 16384 ? YOCO_TC_ST16 : 3);
+        F8 ? (F8_STAGES < 2 ? 2 : F8_STAGES)
+           : (STAGE_BYTES == 16384 ? (QSM ? 3 : YOCO_TC_ST16) : 3);
     static constexpr int SUBE = 128 / ESZ;  // elements per 128-byte row of a sub-tile
     static constexpr int KSUB = D / SUBE;   // 128-byte swizzled sub-tiles per row
     static constexpr int SUB_BYTES = BS * 128;
@@ -94,7 +102,6 @@ struct TcShape {
     // on top of the 128 of the output accumulators: there the queries of the
     // segment sit in shared memory instead (16 rows x D, 16-bit), read per
     // page with ldmatrix.
-    static constexpr bool QSM = D == 256 && NT == 2;
     static constexpr int Q_BYTES = QSM ? 16 * D * 2 : 0;  // per warp
     static constexpr int RING_BYTES = NW * STAGES * STAGE_BYTES;
     static constexpr int SMEM = RING_BYTES + NW * Q_BYTES + 1024;
@@ -609,7 +616,7 @@ __device__ __forceinline__ void cross_cta_merge(const AttnParams& p, const TcWs&
     __syncthreads();
     if (!*ok_flag) return;
 
-    const int half = nseg == 2 ? nthr / 2 : nthr;
+    const int half = nseg == 2 ? nthr / 2 : nthr;  // whole warps: the warp count is even
     const int si = nseg == 2 ? static_cast<int>(threadIdx.x) / half : 0;
     const int tl = static_cast<int>(threadIdx.x) - si * half;  // thread index within the half
     const Seg sg = si == 0 ? sg0 : sg1;
@@ -720,6 +727,9 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
                   "a warp's two end-of-slice pieces must fit in its ring");
     static_assert(!F8 || D % 128 == 0, "e4m3 pages need 128-byte rows");
     static_assert(!RG || !FUSE, "the fused decode step has one row per request");
+    // the cross-CTA merge splits the CTA into two halves for its two segments,
+    // each made of whole warps (its warp shuffles take full masks)
+    static_assert(NW % 2 == 0, "an even number of warps per CTA");
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bars[NW * STAGES];
     __shared__ int32_t stage_blk[NW * STAGES];  // physical page of each stage (-1: invalid)
