@@ -5,15 +5,16 @@
 namespace yoco {
 namespace {
 
-template <bool F8, int NT>
+// Workers (warps, or warp pairs) of the attention kernel for a shape.
+template <bool F8, int NT, bool PR = false>
 int nw_of(int D, int BS) {
     switch (D * 100 + BS) {
-        case 6416: return TcShape<64, 16, F8, NT>::NW;
-        case 6432: return TcShape<64, 32, F8, NT>::NW;
-        case 12816: return TcShape<128, 16, F8, NT>::NW;
-        case 12832: return TcShape<128, 32, F8, NT>::NW;
-        case 25616: return TcShape<256, 16, F8, NT>::NW;
-        default: return TcShape<256, 32, F8, NT>::NW;
+        case 6416: return TcShape<64, 16, F8, NT, PR>::WK;
+        case 6432: return TcShape<64, 32, F8, NT, PR>::WK;
+        case 12816: return TcShape<128, 16, F8, NT, PR>::WK;
+        case 12832: return TcShape<128, 32, F8, NT, PR>::WK;
+        case 25616: return TcShape<256, 16, F8, NT, PR>::WK;
+        default: return TcShape<256, 32, F8, NT, PR>::WK;
     }
 }
 
@@ -28,11 +29,13 @@ size_t tc_workspace_bytes(int sms, int H_kv, int G, int D, int BS, bool e4m3) {
         return static_cast<size_t>(tc_plan_bytes(ctas, nw)) +
                static_cast<size_t>(tc_pieces(ctas, nw, vs)) * (static_cast<size_t>(D) * 4 + 8);
     };
-    // Two 8-head tiles (NT = 2) run for groups wider than 8 and for cross rows
-    // grouped 16 virtual heads wide; one tile for the rest (8 virtual heads at
-    // most). A partial slot holds one tile's heads.
+    // Two 8-head tiles (one warp's, or a warp pair's) run for groups wider than
+    // 8 and for cross rows grouped 16 virtual heads wide; one tile for the rest
+    // (8 virtual heads at most). A partial slot holds one tile's heads.
     const int nw2 = e4m3 ? nw_of<true, 2>(D, BS) : nw_of<false, 2>(D, BS);
-    size_t b = need(nw2, 16);
+    // (the pair shape's workers; shapes without pair kernels have no fewer)
+    const int nwp = e4m3 ? nw_of<true, 1, true>(D, BS) : nw_of<false, 1, true>(D, BS);
+    size_t b = need(nw2 > nwp ? nw2 : nwp, 16);
     if (G <= 8) {
         const int nw1 = e4m3 ? nw_of<true, 1>(D, BS) : nw_of<false, 1>(D, BS);
         const size_t b1 = need(nw1, 8);

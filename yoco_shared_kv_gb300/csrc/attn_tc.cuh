@@ -57,6 +57,13 @@ namespace {
 #ifndef YOCO_TC_ST16
 #define YOCO_TC_ST16 2
 #endif
+// Two-tile walks as warp pairs, per head_dim (1 = on).
+#ifndef YOCO_TC_PAIRS256
+#define YOCO_TC_PAIRS256 1
+#endif
+#ifndef YOCO_TC_PAIRS128
+#define YOCO_TC_PAIRS128 0
+#endif
 // e4m3 cache: warps per CTA and shared-memory bytes of the warps' rings
 // (0 = derived from the piece sizes, below)
 #ifndef YOCO_TC_F8_NW
@@ -67,32 +74,41 @@ namespace {
 #endif
 
 // F8: the cache holds e4m3 bytes (one byte per element) instead of bf16.
-// NT: 8-head tiles of the group (1 for groups up to 8, else 2).
-template <int D, int BS, bool F8 = false, int NT = 2>
+// NT: 8-head tiles of a warp (1 for groups up to 8, else 2).
+// PR: warp pairs (NT = 1): the two warps of a pair walk the same pages from
+// one ring, each taking one of the group's two 8-head tiles, so a 16-column
+// walk runs on twice the warps in the same shared memory.
+template <int D, int BS, bool F8 = false, int NT = 2, bool PR = false>
 struct TcShape {
+    static_assert(!PR || NT == 1, "a warp of a pair takes one 8-head tile");
     static constexpr int ESZ = F8 ? 1 : 2;                // bytes per cached element
     static constexpr int PAGE_BYTES = BS * D * ESZ;       // K (or V) of one page, one kv head
     static constexpr int STAGE_BYTES = 2 * PAGE_BYTES;    // K + V
-    // a warp's two end-of-slice pieces at the largest group of this NT
-    static constexpr int PIECE_PAIR = 2 * (8 * NT * (D * 4 + 8) + 16);
-    // the most warps (8, 4, 2) whose ring share holds two stages and the two pieces
+    static constexpr int NTG = PR ? 2 : NT;               // 8-head tiles of the group
+    // a worker's (warp's, or pair's) two end-of-slice pieces at the largest group
+    static constexpr int PIECE_PAIR = 2 * (8 * NTG * (D * 4 + 8) + 16);
+    // the most workers (8, 4, 2) whose ring share holds two stages and the two pieces
     static constexpr int F8_FITS8 =
         PIECE_PAIR <= YOCO_TC_F8_RING / 8 && 2 * STAGE_BYTES <= YOCO_TC_F8_RING / 8;
     static constexpr int F8_FITS4 =
         PIECE_PAIR <= YOCO_TC_F8_RING / 4 && 2 * STAGE_BYTES <= YOCO_TC_F8_RING / 4;
     static constexpr int F8_NW =
         YOCO_TC_F8_NW > 0 ? YOCO_TC_F8_NW : (F8_FITS8 ? 8 : (F8_FITS4 ? 4 : 2));
-    // Two 8-head tiles at head_dim 256 hold the queries in shared memory (below):
-    // their kernels keep 4 warps x 3 stages whatever the tunables say.
+    // Two 8-head tiles of one warp at head_dim 256 hold the queries in shared
+    // memory (below): their kernels keep 4 warps x 3 stages whatever the
+    // tunables say; so do the pair kernels (4 pairs x 3 stages).
     static constexpr bool QSM = D == 256 && NT == 2;
-    static constexpr int NW =
+    // workers (each with its own ring and slice), and warps
+    static constexpr int WK =
         F8 ? F8_NW
-           : (STAGE_BYTES <= 8192 ? 8 : (STAGE_BYTES <= 16384 ? (QSM ? 4 : YOCO_TC_NW16) : 2));
+           : (STAGE_BYTES <= 8192 ? 8
+                                  : (STAGE_BYTES <= 16384 ? ((QSM || PR) ? 4 : YOCO_TC_NW16) : 2));
+    static constexpr int NW = PR ? 2 * WK : WK;
     // e4m3 pages are small: deepen the ring to keep ~192 KiB in flight per SM
     static constexpr int F8_STAGES = YOCO_TC_F8_RING / F8_NW / STAGE_BYTES;
     static constexpr int STAGES =
         F8 ? (F8_STAGES < 2 ? 2 : F8_STAGES)
-           : (STAGE_BYTES == 16384 ? (QSM ? 3 : YOCO_TC_ST16) : 3);
+           : (STAGE_BYTES == 16384 ? ((QSM || PR) ? 3 : YOCO_TC_ST16) : 3);
     static constexpr int SUBE = 128 / ESZ;  // elements per 128-byte row of a sub-tile
     static constexpr int KSUB = D / SUBE;   // 128-byte swizzled sub-tiles per row
     static constexpr int SUB_BYTES = BS * 128;
@@ -103,7 +119,7 @@ struct TcShape {
     // segment sit in shared memory instead (16 rows x D, 16-bit), read per
     // page with ldmatrix.
     static constexpr int Q_BYTES = QSM ? 16 * D * 2 : 0;  // per warp
-    static constexpr int RING_BYTES = NW * STAGES * STAGE_BYTES;
+    static constexpr int RING_BYTES = WK * STAGES * STAGE_BYTES;
     static constexpr int SMEM = RING_BYTES + NW * Q_BYTES + 1024;
     static_assert(SMEM <= 225 * 1024, "the rings must leave room for static shared memory");
 };
@@ -717,39 +733,50 @@ __device__ __forceinline__ void cross_cta_merge(const AttnParams& p, const TcWs&
 // RG: cross rows grouped on one walk (p.rg > 1; FUSE = false only).
 // Without it every segment is one row and the per-column causal masks and
 // the guard for columns without keys compile away.
-template <int D, int BS, int NT, bool REV, bool F8, bool FUSE, bool RG>
-__global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
+// PR: warp pairs (NT = 1, FUSE = false): a worker is two warps that walk one
+// slice from one ring, warp 2k taking columns 0-7 of the group and warp
+// 2k + 1 columns 8-15. The pair's leader issues the copies; both wait on them
+// and agree on every outcome through one pair barrier, so that they always
+// take the same path.
+template <int D, int BS, int NT, bool REV, bool F8, bool FUSE, bool RG, bool PR>
+__global__ void __launch_bounds__(TcShape<D, BS, F8, NT, PR>::NW * 32, 1)
     attn_tc_persistent(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
-    using S = TcShape<D, BS, F8, NT>;
-    constexpr int NW = S::NW, STAGES = S::STAGES;
+    using S = TcShape<D, BS, F8, NT, PR>;
+    constexpr int NW = S::NW, WK = S::WK, STAGES = S::STAGES, NTG = S::NTG;
     static_assert(S::PIECE_PAIR <= STAGES * S::STAGE_BYTES,
-                  "a warp's two end-of-slice pieces must fit in its ring");
+                  "a worker's two end-of-slice pieces must fit in its ring");
     static_assert(!F8 || D % 128 == 0, "e4m3 pages need 128-byte rows");
     static_assert(!RG || !FUSE, "the fused decode step has one row per request");
+    static_assert(!PR || !FUSE, "the fused decode step runs one warp per ring");
     // the cross-CTA merge splits the CTA into two halves for its two segments,
     // each made of whole warps (its warp shuffles take full masks)
     static_assert(NW % 2 == 0, "an even number of warps per CTA");
+    static_assert(WK <= 15, "one named barrier per pair");
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[NW * STAGES];
-    __shared__ int32_t stage_blk[NW * STAGES];  // physical page of each stage (-1: invalid)
+    __shared__ __align__(8) uint64_t bars[WK * STAGES];
+    __shared__ int32_t stage_blk[WK * STAGES];  // physical page of each stage (-1: invalid)
     // e4m3: the page's scale record {k_scale, v_scale, -, -}, copied with the page
-    __shared__ __align__(16) float4 stage_scale[F8 ? NW * STAGES : 1];
-    __shared__ PieceHdr hdr[NW][2];
+    __shared__ __align__(16) float4 stage_scale[F8 ? WK * STAGES : 1];
+    __shared__ PieceHdr hdr[WK][2];
     __shared__ int abort_flag;
     __shared__ __align__(16) CtaHdr cta_hdr;  // this CTA's first / last segment (from the plan)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gl = lane >> 2, tq = lane & 3;  // mma fragment row group / column pair
-    const TcWs ws = tc_ws(p, gridDim.x, NW, D);
+    const int wk = PR ? warp >> 1 : warp;    // this warp's worker
+    const int c8 = PR ? (warp & 1) * 8 : 0;  // first column of the group this warp takes
+    const bool leader = !PR || (warp & 1) == 0;
+    const int pair_bar = 1 + wk;             // the pair's named barrier (PR)
+    const TcWs ws = tc_ws(p, gridDim.x, WK, D);
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
-    uint8_t* wbuf = smem + warp * STAGES * S::STAGE_BYTES;
-    uint64_t* wbar = bars + warp * STAGES;
-    if (lane == 0) {  // each warp's own ring barriers: only this warp waits on them
+    uint8_t* wbuf = smem + wk * STAGES * S::STAGE_BYTES;
+    uint64_t* wbar = bars + wk * STAGES;
+    if (lane == 0 && leader) {  // each worker's ring barriers: only its warps wait on them
         for (int i = 0; i < STAGES; ++i) mbar_init(&wbar[i], 1);
         fence_mbar_init();
-        hdr[warp][0].valid = hdr[warp][1].valid = 0;
+        hdr[wk][0].valid = hdr[wk][1].valid = 0;
     }
     __syncwarp();
     // This warp's plan record (the forward or the reverse walk): four
@@ -758,8 +785,8 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
     uint4 r0, r1, r2, r3;
     {
         const uint4* src = reinterpret_cast<const uint4*>(
-            ws.wplan + (REV ? static_cast<int64_t>(gridDim.x) * NW : 0) +
-            static_cast<int64_t>(blockIdx.x) * NW + warp);
+            ws.wplan + (REV ? static_cast<int64_t>(gridDim.x) * WK : 0) +
+            static_cast<int64_t>(blockIdx.x) * WK + wk);
         r0 = __ldg(src);
         r1 = __ldg(src + 1);
         r2 = __ldg(src + 2);
@@ -794,15 +821,15 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i) cd[i] = c[i];
         plan_state = launch_aborted(p) ? 1
-                     : plan_matches(ph, p, D, BS, NW, STAGES, static_cast<int>(gridDim.x)) ? 0 : 2;
+                     : plan_matches(ph, p, D, BS, WK, STAGES, static_cast<int>(gridDim.x)) ? 0 : 2;
     }
     const int64_t P = static_cast<int64_t>((static_cast<uint64_t>(r0.y) << 32) | r0.x);
     const int64_t C = gridDim.x;
     const int64_t cta_lo = P * blockIdx.x / C, cta_hi = P * (blockIdx.x + 1) / C;
-    const int64_t my_lo = cta_lo + (cta_hi - cta_lo) * warp / NW;
-    const int64_t my_hi = cta_lo + (cta_hi - cta_lo) * (warp + 1) / NW;
+    const int64_t my_lo = cta_lo + (cta_hi - cta_lo) * wk / WK;
+    const int64_t my_hi = cta_lo + (cta_hi - cta_lo) * (wk + 1) / WK;
     int32_t n_my = static_cast<int32_t>(my_hi - my_lo);
-    const int32_t wid = blockIdx.x * NW + warp;
+    const int32_t wid = blockIdx.x * WK + wk;
     const int64_t cap64 = static_cast<int64_t>(p.max_blocks) * BS;
     const int32_t cap = cap64 > 0x7fffffff ? 0x7fffffff : static_cast<int32_t>(cap64);
 
@@ -850,13 +877,13 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
     const uint64_t pol_keep = keep_tail ? make_l2_policy_evict_last() : 0;
     const uint64_t pol_stream = keep_tail ? make_l2_policy_evict_first() : 0;
     const int keep_pages = static_cast<int>(
-        kKeepBytes / (static_cast<int64_t>(gridDim.x) * NW * S::STAGE_BYTES));
-    auto issue = [&](int i) {  // lane 0 only; pc is at page i, blk_next its entry
+        kKeepBytes / (static_cast<int64_t>(gridDim.x) * WK * S::STAGE_BYTES));
+    auto issue = [&](int i) {  // the worker's lane 0 only; pc is at page i, blk_next its entry
         const int st = i % STAGES;
         uint64_t* bar = wbar + st;
         const int32_t blk = blk_next;
         // published to the consumer lanes by the barrier's release/acquire
-        stage_blk[warp * STAGES + st] = (blk < 0 || blk >= p.num_blocks) ? -1 : blk;
+        stage_blk[wk * STAGES + st] = (blk < 0 || blk >= p.num_blocks) ? -1 : blk;
         if (blk < 0 || blk >= p.num_blocks) {
             set_err(p.err, YOCO_DEVERR_PAGE_RANGE);
             mbar_arrive(bar);
@@ -880,13 +907,13 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
                 }
             }
             if constexpr (F8)
-                bulk_load(&stage_scale[warp * STAGES + st],
+                bulk_load(&stage_scale[wk * STAGES + st],
                           p.scales + static_cast<int64_t>(blk) * p.H_kv + pc.g, 16, bar);
         }
         step(pc);
     };
     const int pro = n_my < STAGES ? n_my : STAGES;
-    if (lane == 0) {
+    if (lane == 0 && leader) {
         // the prologue's pages take their block ids from the plan
 #pragma unroll
         for (int i = 0; i < STAGES; ++i) {
@@ -1075,13 +1102,13 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
         } else {
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                const int h = nt * 8 + gl;
+                const int h = c8 + nt * 8 + gl;
                 bool ok;
                 int hr = 0, hh = 0;
                 if constexpr (RG) {
 #pragma unroll
                     for (int e = 0; e < 2; ++e)
-                        moff[nt][e] = nr - 1 - min((nt * 8 + 2 * tq + e) / p.G, nr - 1);
+                        moff[nt][e] = nr - 1 - min((c8 + nt * 8 + 2 * tq + e) / p.G, nr - 1);
                     ok = h < nr * p.G;
                     hr = ok ? h / p.G : 0;
                     hh = ok ? h - hr * p.G : 0;
@@ -1146,19 +1173,21 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
             if (fused) load_patch(cc.req, cc.g);
         }
         const int st = i % STAGES;
-        if (!mbar_wait_bounded(wbar + st, (i / STAGES) & 1, kWaitLimitNs)) {
+        bool landed = mbar_wait_bounded(wbar + st, (i / STAGES) & 1, kWaitLimitNs);
+        if constexpr (PR) landed = pair_all(pair_bar, landed);  // both warps or neither
+        if (!landed) {
             aborted = true;
             break;
         }
         consumed = i + 1;
-        if (stage_blk[warp * STAGES + st] >= 0) {
+        if (stage_blk[wk * STAGES + st] >= 0) {
             const uint32_t kbase = smem_u32(wbuf + st * S::STAGE_BYTES);
             const uint32_t vbase = kbase + S::PAGE_BYTES;
             const int32_t nvalid = min(BS, cc.kv_len - cc.pp * BS);
             float sl2p = sl2, vr = 1.f;  // score factor, weight factor of this page
             if constexpr (F8) {
                 // codes widen exactly; the page's K scale goes into the score factor
-                const float4 sc4 = stage_scale[warp * STAGES + st];
+                const float4 sc4 = stage_scale[wk * STAGES + st];
                 if (lane == 0 && !(sc4.x >= 0x1p-16f && sc4.x <= 128.f && sc4.y >= 0x1p-16f &&
                                    sc4.y <= 128.f))
                     set_err(p.err, YOCO_DEVERR_SCALE);
@@ -1191,7 +1220,7 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
                 if (lane < PCH) {
                     uint4 kw, vw;
                     if constexpr (F8) {
-                        const float4 sc4 = stage_scale[warp * STAGES + st];
+                        const float4 sc4 = stage_scale[wk * STAGES + st];
                         const uint2 k0 = quantise8_e4m3(pk[0], sc4.x), k1 = quantise8_e4m3(pk[PIN - 1], sc4.x);
                         const uint2 v0 = quantise8_e4m3(pv[0], sc4.y), v1 = quantise8_e4m3(pv[PIN - 1], sc4.y);
                         kw = make_uint4(k0.x, k0.y, k1.x, k1.y);
@@ -1210,14 +1239,16 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
             if (nvalid < BS) {
                 // Rows past the causal end may hold stale data (even NaN), and a
                 // zero probability times NaN is NaN: clear those V rows first.
+                // (a pair's warps clear alternate sub-tiles, then meet)
                 uint8_t* vd = wbuf + st * S::STAGE_BYTES + S::PAGE_BYTES;
                 const int nbytes = (BS - nvalid) * 128;
-                for (int c = 0; c < S::KSUB; ++c)
+                for (int c = PR ? (warp & 1) : 0; c < S::KSUB; c += PR ? 2 : 1)
                     for (int b = lane * 16; b < nbytes; b += 32 * 16)
                         *reinterpret_cast<uint4*>(vd + c * S::SUB_BYTES + nvalid * 128 + b) =
                             make_uint4(0, 0, 0, 0);
                 fence_proxy_async_smem();
-                __syncwarp();
+                if constexpr (PR) pair_sync(pair_bar);
+                else __syncwarp();
             }
             // ---- S^T = K Q^T (tokens x heads); two accumulators halve the chain ----
             float sc[S::MT][NT][4];
@@ -1494,8 +1525,10 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
                 }
             }
         }
-        __syncwarp();
-        if (lane == 0 && i + STAGES < n_my) {
+        // the stage is free once every warp reading it is done (both of a pair)
+        if constexpr (PR) pair_sync(pair_bar);
+        else __syncwarp();
+        if (lane == 0 && leader && i + STAGES < n_my) {
             issue(i + STAGES);
             if (i + STAGES + 1 < n_my) fetch_blk();
         }
@@ -1511,13 +1544,13 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
             const int64_t s0 = cc.seg_start, s1 = cc.seg_start + cc.pages;
             const int nvh = RG ? cc.nr * p.G : p.G;  // virtual heads of the group (row-major over its rows)
             if (s0 >= my_lo && s1 <= my_hi) {
-                // whole segment in this warp: final output
+                // whole segment in this worker: final output
                 __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        const int h = nt * 8 + 2 * tq + e;
+                        const int h = c8 + nt * 8 + 2 * tq + e;
                         // a group row without any key (seq_len below its request's rows)
                         // is zero-filled and flagged above: never written here
                         if (h >= nvh || (RG && l_part[nt][e] == 0.f)) continue;
@@ -1553,7 +1586,7 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        const int h = nt * 8 + 2 * tq + e;
+                        const int h = c8 + nt * 8 + 2 * tq + e;
                         if (h >= nvh) continue;
                         float* dst = dst_o + h * D;
                         const float of = F8 ? vref : 1.f;  // partials in true units
@@ -1564,15 +1597,15 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
                         }
                         if (gl == 0) dst_ml[h] = make_float2(m_run[nt][e], l_part[nt][e]);
                     }
-                if (lane == 0) {
-                    hdr[warp][slot].s0 = s0;
-                    hdr[warp][slot].s1 = s1;
-                    hdr[warp][slot].n = cc.n;
-                    hdr[warp][slot].g = cc.g;
-                    hdr[warp][slot].nr = cc.nr;
-                    hdr[warp][slot].o = dst_o;
-                    hdr[warp][slot].ml = dst_ml;
-                    hdr[warp][slot].valid = 1;
+                if (lane == 0 && leader) {
+                    hdr[wk][slot].s0 = s0;
+                    hdr[wk][slot].s1 = s1;
+                    hdr[wk][slot].n = cc.n;
+                    hdr[wk][slot].g = cc.g;
+                    hdr[wk][slot].nr = cc.nr;
+                    hdr[wk][slot].o = dst_o;
+                    hdr[wk][slot].ml = dst_ml;
+                    hdr[wk][slot].valid = 1;
                 }
             }
             reset_state();
@@ -1581,7 +1614,7 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
     }
 
     if (aborted) {
-        // drain this warp's copies still in flight before the CTA exits
+        // drain the copies of this worker still in flight before the CTA exits
         const int issued = n_my < consumed + STAGES ? n_my : consumed + STAGES;
         for (int i = consumed; i < issued; ++i)
             (void)mbar_wait_bounded(wbar + (i % STAGES), (i / STAGES) & 1, kWaitLimitNs);
@@ -1593,8 +1626,8 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
     __syncthreads();  // pieces and headers are visible to the whole CTA
     if (abort_flag) return;
 
-    // ---- combine the pieces of each segment this CTA holds, in warp order ----
-    // A group is the run of valid pieces (warp, then slot order) of one
+    // ---- combine the pieces of each segment this CTA holds, in worker order ----
+    // A group is the run of valid pieces (worker, then slot order) of one
     // segment. Every thread walks the groups itself and derives the scale
     // factors it needs, so the combine has no barrier and no serial step: it
     // runs once per launch, right after streaming, with a cold instruction
@@ -1604,7 +1637,7 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
     // groups lay the threads out head-major, each taking one head and every
     // tph-th vector of it, so the factors are derived once per head, not once
     // per vector.
-    constexpr int MAXE = 2 * NW;
+    constexpr int MAXE = 2 * WK;
     constexpr int D4 = D / 4;  // four-element vectors per head
     __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out);
     const int VS = p.vhs;       // virtual heads per partial slot
@@ -1615,18 +1648,18 @@ __global__ void __launch_bounds__(TcShape<D, BS, F8, NT>::NW * 32, 1)
     int e0 = 0;
     for (;;) {
         while (e0 < MAXE && !hdr[e0 >> 1][e0 & 1].valid) ++e0;
-        if (e0 >= MAXE || (NT != 1 && !RG && ch >= p.G)) break;
+        if (e0 >= MAXE || (NTG != 1 && !RG && ch >= p.G)) break;
         const int64_t s0 = hdr[e0 >> 1][e0 & 1].s0, s1 = hdr[e0 >> 1][e0 & 1].s1;
         const int32_t gn = hdr[e0 >> 1][e0 & 1].n, gg = hdr[e0 >> 1][e0 & 1].g;
         const int32_t gnr = hdr[e0 >> 1][e0 & 1].nr;
         int e1 = e0 + 1;  // one past the group (entries in between may be invalid)
         while (e1 < MAXE && (!hdr[e1 >> 1][e1 & 1].valid || hdr[e1 >> 1][e1 & 1].s0 == s0)) ++e1;
-        if (NT != 1 && RG && ch >= gnr * p.G) {  // no head of this thread in the group
+        if (NTG != 1 && RG && ch >= gnr * p.G) {  // no head of this thread in the group
             e0 = e1;
             continue;
         }
         const bool whole = s0 >= cta_lo && s1 <= cta_hi;
-        if constexpr (NT == 1) {
+        if constexpr (NTG == 1) {
             const int cslot = s0 < cta_lo ? 0 : 1;
             // groups of rows (one 8-head tile) are laid out row-major: virtual head h
             // is head h % G of row gn + h / G
@@ -1747,16 +1780,19 @@ cudaError_t ensure_smem_attr(K kernel, int bytes, unsigned long long& done) {
     return e;
 }
 
-template <int D, int BS, int NT, bool F8>
+template <int D, int BS, int NT, bool F8, bool PR>
 cudaError_t launch_one(const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p, int sms,
                        cudaStream_t s) {
-    using S = TcShape<D, BS, F8, NT>;
+    using S = TcShape<D, BS, F8, NT, PR>;
     static unsigned long long smem_fwd = 0, smem_rev = 0, smem_fuse = 0;  // one per kernel
     static unsigned long long smem_gfwd = 0, smem_grev = 0;
     const int ctas = tc_ctas(sms);
     // the cross-CTA merge keeps its tables in the (then idle) ring
     if ((16 + 2 * merge_scratch_floats(ctas, 16, D)) * 4 > S::SMEM - 1024)
         return cudaErrorInvalidConfiguration;
+    const bool fuse = p.k_new != nullptr, grouped = p.rg > 1;
+    if (grouped && fuse) return cudaErrorInvalidConfiguration;
+    if (PR && fuse) return cudaErrorInvalidConfiguration;  // the fused step runs one warp per ring
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -1767,23 +1803,33 @@ cudaError_t launch_one(const CUtensorMap& mk, const CUtensorMap& mv, const AttnP
     cfg.attrs = attr;
     cudaError_t e;
     if (!p.planned) {
-        // The step's plan. It may start while the previous kernel drains when
-        // the caller allows the overlap (it reads only the metadata before its
-        // dependency wait); the attention launch below reads the plan at its
-        // very start, so it is an ordinary (fully ordered) launch.
+        // The step's plan (one warp per worker). It may start while the
+        // previous kernel drains when the caller allows the overlap (it reads
+        // only the metadata before its dependency wait); the attention launch
+        // below reads the plan at its very start, so it is an ordinary (fully
+        // ordered) launch.
         cfg.dynamicSmemBytes = 0;
+        cfg.blockDim = dim3(S::WK * 32);
         cfg.numAttrs = p.overlap ? 1 : 0;
-        e = cudaLaunchKernelEx(&cfg, attn_tc_plan<S::NW, S::STAGES, D, BS>, p);
+        e = cudaLaunchKernelEx(&cfg, attn_tc_plan<S::WK, S::STAGES, D, BS>, p);
         if (e != cudaSuccess || p.plan_only) return e;
+        cfg.blockDim = dim3(S::NW * 32);
     }
-    const bool fuse = p.k_new != nullptr, grouped = p.rg > 1;
-    if (grouped && fuse) return cudaErrorInvalidConfiguration;
-    // row groups: kernels of their own
-    auto kernel = fuse ? attn_tc_persistent<D, BS, NT, false, F8, true, false>
-                  : grouped ? (p.reverse ? attn_tc_persistent<D, BS, NT, true, F8, false, true>
-                                         : attn_tc_persistent<D, BS, NT, false, F8, false, true>)
-                            : (p.reverse ? attn_tc_persistent<D, BS, NT, true, F8, false, false>
-                                         : attn_tc_persistent<D, BS, NT, false, F8, false, false>);
+    // row groups and warp pairs: kernels of their own
+    using K = void (*)(CUtensorMap, CUtensorMap, AttnParams);
+    K kernel;
+    if constexpr (PR) {
+        kernel = grouped ? (p.reverse ? attn_tc_persistent<D, BS, NT, true, F8, false, true, true>
+                                      : attn_tc_persistent<D, BS, NT, false, F8, false, true, true>)
+                         : (p.reverse ? attn_tc_persistent<D, BS, NT, true, F8, false, false, true>
+                                      : attn_tc_persistent<D, BS, NT, false, F8, false, false, true>);
+    } else {
+        kernel = fuse ? attn_tc_persistent<D, BS, NT, false, F8, true, false, false>
+                 : grouped ? (p.reverse ? attn_tc_persistent<D, BS, NT, true, F8, false, true, false>
+                                        : attn_tc_persistent<D, BS, NT, false, F8, false, true, false>)
+                           : (p.reverse ? attn_tc_persistent<D, BS, NT, true, F8, false, false, false>
+                                        : attn_tc_persistent<D, BS, NT, false, F8, false, false, false>);
+    }
     unsigned long long& done = fuse ? smem_fuse
                                : grouped ? (p.reverse ? smem_grev : smem_gfwd)
                                          : (p.reverse ? smem_rev : smem_fwd);
@@ -1799,14 +1845,30 @@ cudaError_t launch_one(const CUtensorMap& mk, const CUtensorMap& mv, const AttnP
     return cudaLaunchKernelEx(&cfg, kernel, mk, mv, p);
 }
 
+// Two-tile walks (groups over 8 heads, or rows grouped 16 wide) run as warp
+// pairs at these head dims, except the fused decode step (one warp per ring),
+// where a pair kernel has at most 8 warps (registers for the one-tile walk).
+template <int D, int BS, bool F8>
+constexpr bool tc_pairs() {
+    return (D == 256 ? YOCO_TC_PAIRS256 != 0 : D == 128 ? YOCO_TC_PAIRS128 != 0 : false) &&
+           TcShape<D, BS, F8, 1, true>::NW <= 8;
+}
+
+template <int D, int BS, bool F8>
+cudaError_t launch_bs(const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p, int sms,
+                      cudaStream_t s) {
+    const bool wide = p.vhs > 8;  // two 8-head tiles: a group over 8, or 16 virtual heads
+    if constexpr (tc_pairs<D, BS, F8>()) {
+        if (wide && p.k_new == nullptr) return launch_one<D, BS, 1, F8, true>(mk, mv, p, sms, s);
+    }
+    return wide ? launch_one<D, BS, 2, F8, false>(mk, mv, p, sms, s)
+                : launch_one<D, BS, 1, F8, false>(mk, mv, p, sms, s);
+}
+
 template <int D, bool F8>
 cudaError_t launch_d(const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p, int BS,
                      int sms, cudaStream_t s) {
-    const bool wide = p.vhs > 8;  // two 8-head tiles: a group over 8, or 16 virtual heads
-    if (BS == 16) return wide ? launch_one<D, 16, 2, F8>(mk, mv, p, sms, s)
-                              : launch_one<D, 16, 1, F8>(mk, mv, p, sms, s);
-    return wide ? launch_one<D, 32, 2, F8>(mk, mv, p, sms, s)
-                : launch_one<D, 32, 1, F8>(mk, mv, p, sms, s);
+    return BS == 16 ? launch_bs<D, 16, F8>(mk, mv, p, sms, s) : launch_bs<D, 32, F8>(mk, mv, p, sms, s);
 }
 
 }  // namespace

@@ -169,6 +169,27 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+// Named barrier of two warps (64 threads; id 1..15, 0 is __syncthreads). Both
+// warps must reach it the same number of times.
+__device__ __forceinline__ void pair_sync(int id) {
+    asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
+}
+
+// The same barrier, returning the AND of the 64 threads' predicates: both
+// warps leave with the same answer.
+__device__ __forceinline__ bool pair_all(int id, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{ .reg .pred p, q;\n"
+        "  setp.ne.u32 p, %1, 0;\n"
+        "  bar.red.and.pred q, %2, 64, p;\n"
+        "  selp.u32 %0, 1, 0, q; }"
+        : "=r"(r)
+        : "r"(v ? 1u : 0u), "r"(id)
+        : "memory");
+    return r != 0;
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
