@@ -392,11 +392,26 @@ def test_fp32_rows_beyond_max_seq_len_are_cut_and_flagged(P, N, max_seq_len):
     assert np.abs(got - ref).max() <= ATOL["f32"]
 
 
-@pytest.mark.parametrize("idx", [1, 2, 3, 4])
+def _pair_workload(kind):
+    """Workloads whose walks run on warp pairs (two 8-head tiles at head_dim 256)."""
+    from workloads import spec_decode
+    if kind == "wide":  # 16 query heads per kv head
+        return pure_decode(8200, num_reqs=5, ctx_lo=1, ctx_hi=700, H_q=32, H_kv=2, D=256, bs=16,
+                           layers=2)
+    # four rows of a request at four heads per kv head: 16-wide row groups
+    return spec_decode(8300, num_reqs=5, ctx_lo=1, ctx_hi=700, draft=4, layers=2)
+
+
+def _workload(idx):
+    return _pair_workload(idx) if isinstance(idx, str) else SMALL[idx]()
+
+
+@pytest.mark.parametrize("idx", [1, 2, 3, 4, "wide", "spec"])
 def test_planned_layers_equal_unplanned_calls(P, N, idx):
     """A layer reusing the step's plan (YOCO_ATTN_PLANNED) gives the same bits as
-    a self-contained call that makes its own plan first, for both page walks."""
-    wl = SMALL[idx]()
+    a self-contained call that makes its own plan first, for both page walks (also
+    on the warp-pair kernels)."""
+    wl = _workload(idx)
     dw = P.DeviceWorkload(wl, alternate=True)
     dw.run_all()
     torch.cuda.synchronize()
@@ -415,10 +430,12 @@ def test_planned_layers_equal_unplanned_calls(P, N, idx):
     assert np.abs(gpu_out(ds.out) - ref).max() <= ATOL["bf16"]
 
 
-def test_planned_call_without_a_matching_plan_is_refused(P, N):
+@pytest.mark.parametrize("idx", [1, "wide", "spec"])
+def test_planned_call_without_a_matching_plan_is_refused(P, N, idx):
     """YOCO_ATTN_PLANNED on a workspace that holds no plan, or a plan made for
-    other shapes: the launch writes nothing and sets YOCO_DEVERR_PLAN."""
-    wl = SMALL[1]()
+    other shapes: the launch writes nothing and sets YOCO_DEVERR_PLAN (one warp per
+    ring, and warp pairs: both warps of a pair leave together)."""
+    wl = _workload(idx)
     dw = P.DeviceWorkload(wl)
     dw.run_all()
     torch.cuda.synchronize()
