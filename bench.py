@@ -24,6 +24,7 @@ import hashlib
 import io
 import json
 import os
+import re
 import subprocess
 import sys
 import time
@@ -161,12 +162,26 @@ def measured_peaks() -> dict:
 KERNEL_SOURCES = ("attn_tc.cuh", "attn_tc.cu", "attn_tc_e4m3.cu", "attn_common.cuh", "common.cuh")
 
 
+def _code_only(text: str) -> str:
+    """C++/CUDA source without its comments and blank lines."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    out = []
+    for line in text.splitlines():
+        cut = line.find("//")
+        if cut >= 0:
+            line = line[:cut]
+        if line.strip():
+            out.append(line.rstrip())
+    return "\n".join(out)
+
+
 def kernel_source_sha() -> str:
-    """Hash of the sources the dominant kernel is built from."""
+    """Hash of the code the dominant kernel is built from (comments and blank
+    lines left out: editing a comment does not change the kernel)."""
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "yoco_shared_kv_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "yoco_shared_kv_gb300", "csrc", name), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

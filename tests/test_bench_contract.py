@@ -71,3 +71,12 @@ def test_reference_config_matches_the_gpu_arm(capsys, monkeypatch):
     wl = bench.make_workload(0)
     st = wl.steps[-1]
     assert d["config"] == bench.workload_config(wl, st, bench.accounting(wl, st), 1)
+
+
+def test_kernel_hash_ignores_comments_only():
+    """The traffic figures stay attached to the kernel's code: a comment or blank-line
+    edit keeps the hash, any code edit changes it."""
+    import bench
+    src = "int a = 1;  // one\n/* block\n comment */\n\nint b = 2;\n"
+    assert bench._code_only(src) == bench._code_only("int a = 1;\n// other words\nint b = 2;\n")
+    assert bench._code_only(src) != bench._code_only("int a = 1;\nint b = 3;\n")

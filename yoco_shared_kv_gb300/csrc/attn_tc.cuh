@@ -11,14 +11,16 @@
 // Work decomposition. The unit of work is a page of one (cross row, kv head)
 // segment. Segments are laid out in the order (row, kv head) and their pages
 // form one flattened sequence of P pages. The grid has one CTA per SM; CTA c
-// owns pages [P c / C, P (c+1) / C) and each of its NW warps owns an equal
-// contiguous slice of that, streamed through the warp's own TMA ring. Every
-// worker therefore moves the same number of bytes, whatever the length mix,
-// and the ring never drains between segments. Where each warp's slice starts
-// is worked out once per step (attn_tc_plan) and read by every layer.
-//   - A segment that lies inside one warp's slice is finished in registers
+// owns pages [P c / C, P (c+1) / C) and each of its workers owns an equal
+// contiguous slice of that, streamed through the worker's own TMA ring. A
+// worker is a warp, or (PR) a pair of warps that share the ring and split
+// the group's 16 columns. Every worker therefore moves the same number of
+// bytes, whatever the length mix, and the ring never drains between
+// segments. Where each worker's slice starts is worked out once per step
+// (attn_tc_plan) and read by every layer.
+//   - A segment that lies inside one worker's slice is finished in registers
 //     and written straight to `out`.
-//   - A segment cut by a warp boundary leaves a partial (m, l, o) per piece;
+//   - A segment cut by a worker boundary leaves a partial (m, l, o) per piece;
 //     at the end of the kernel the CTA combines the pieces of each segment
 //     it holds, writing `out` when the CTA holds the whole segment and a
 //     CTA-level partial otherwise.
@@ -439,7 +441,7 @@ __device__ void plan_walk(const AttnParams& p, int lane, int64_t P, int64_t lo, 
     }
 }
 
-// The per-step plan: one CTA per attention CTA, one warp per attention warp.
+// The per-step plan: one CTA per attention CTA, one warp per attention worker.
 // Reads the metadata, then (after the dependency wait, since the previous
 // kernel may be a layer still using the workspace) writes the records, the
 // CTA headers and zeroes the arrival counters.
