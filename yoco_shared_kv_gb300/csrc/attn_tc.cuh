@@ -1782,6 +1782,15 @@ cudaError_t ensure_smem_attr(K kernel, int bytes, unsigned long long& done) {
     return e;
 }
 
+// Two-tile walks (groups over 8 heads, or rows grouped 16 wide) run as warp
+// pairs at these head dims, except the fused decode step (one warp per ring),
+// where a pair kernel has at most 8 warps (registers for the one-tile walk).
+template <int D, int BS, bool F8>
+constexpr bool tc_pairs() {
+    return (D == 256 ? YOCO_TC_PAIRS256 != 0 : D == 128 ? YOCO_TC_PAIRS128 != 0 : false) &&
+           TcShape<D, BS, F8, 1, true>::NW <= 8;
+}
+
 template <int D, int BS, int NT, bool F8, bool PR>
 cudaError_t launch_one(const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p, int sms,
                        cudaStream_t s) {
@@ -1817,10 +1826,14 @@ cudaError_t launch_one(const CUtensorMap& mk, const CUtensorMap& mv, const AttnP
         if (e != cudaSuccess || p.plan_only) return e;
         cfg.blockDim = dim3(S::NW * 32);
     }
-    // row groups and warp pairs: kernels of their own
+    // row groups and warp pairs: kernels of their own. Where two-tile walks run
+    // as warp pairs, a one-warp two-tile kernel serves the fused step alone.
     using K = void (*)(CUtensorMap, CUtensorMap, AttnParams);
     K kernel;
-    if constexpr (PR) {
+    if constexpr (!PR && NT == 2 && tc_pairs<D, BS, F8>()) {
+        if (!fuse) return cudaErrorInvalidConfiguration;
+        kernel = attn_tc_persistent<D, BS, NT, false, F8, true, false, false>;
+    } else if constexpr (PR) {
         kernel = grouped ? (p.reverse ? attn_tc_persistent<D, BS, NT, true, F8, false, true, true>
                                       : attn_tc_persistent<D, BS, NT, false, F8, false, true, true>)
                          : (p.reverse ? attn_tc_persistent<D, BS, NT, true, F8, false, false, true>
@@ -1845,15 +1858,6 @@ cudaError_t launch_one(const CUtensorMap& mk, const CUtensorMap& mv, const AttnP
     cfg.dynamicSmemBytes = S::SMEM;
     cfg.numAttrs = (p.planned && p.overlap) ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kernel, mk, mv, p);
-}
-
-// Two-tile walks (groups over 8 heads, or rows grouped 16 wide) run as warp
-// pairs at these head dims, except the fused decode step (one warp per ring),
-// where a pair kernel has at most 8 warps (registers for the one-tile walk).
-template <int D, int BS, bool F8>
-constexpr bool tc_pairs() {
-    return (D == 256 ? YOCO_TC_PAIRS256 != 0 : D == 128 ? YOCO_TC_PAIRS128 != 0 : false) &&
-           TcShape<D, BS, F8, 1, true>::NW <= 8;
 }
 
 template <int D, int BS, bool F8>
