@@ -248,3 +248,24 @@ def test_plan_host_validation(lib_path):
     assert plan(dt=N.YOCO_E4M3, d=64) == N.YOCO_ERR_UNSUPPORTED      # e4m3 pages need 128-byte rows
     assert plan(hq=17, hkv=1) == N.YOCO_ERR_UNSUPPORTED
     assert plan(dt=N.YOCO_F32, ws=None, ws_bytes=0, hq=8, hkv=2) == N.YOCO_OK  # no plan needed
+
+
+def test_noalloc_array_holds_every_tensor_core_shape(lib_path):
+    """The attention workspace of the bf16 and e4m3 paths does not depend on context
+    length or row count, and for every supported bf16 head_dim, block size and group
+    (one row per request or row groups, one warp per ring or warp pairs) it fits the
+    allocation-free entry's fixed array."""
+    import torch
+    from yoco_shared_kv_gb300 import _native as N
+    cap = N.yoco_cross_attn_noalloc_capacity()
+    for dt in (torch.bfloat16, torch.float8_e4m3fn):
+        for D in (64, 128, 256):
+            if dt is torch.float8_e4m3fn and D == 64:
+                continue  # e4m3 pages need 128-byte rows
+            for bs in (16, 32):
+                for G in (1, 2, 3, 4, 8, 12, 16):
+                    need = N.yoco_cross_attn_workspace_size(64, G * 2, 2, D, bs, 1 << 20, dt)
+                    assert need > 0, (dt, D, bs, G)
+                    assert need == N.yoco_cross_attn_workspace_size(4096, G * 2, 2, D, bs, 512, dt)
+                    if dt is torch.bfloat16:
+                        assert need <= cap, (D, bs, G, need)

@@ -134,3 +134,33 @@ def test_full_size_speculative_rows(P):
     layers = [0, wl.layers - 1]
     ref = oracle_step_out(wl, step, layers=layers, rows=rows)
     assert np.abs(got[layers][:, rows] - ref).max() <= ATOL["bf16"]
+
+
+def test_full_size_speculative_rows_e4m3(P):
+    """The speculative workload over the e4m3 cache at full size: the 16-wide row
+    groups on warp pairs; sampled rows x layers against the oracle over the dequantised
+    cache, and an odd layer (backward walk) recomputed bit for bit."""
+    from tests.helpers import oracle_e4m3_pools, oracle_e4m3_step_out
+    from workloads import MULTI_ROW_FULL, page_scales
+    wl = MULTI_ROW_FULL()
+    sc = page_scales(wl)
+    dw = P.DeviceWorkload(wl, kv="e4m3", page_scales=sc)
+    dw.run_fill()
+    dw.run_step(0)
+    torch.cuda.synchronize()
+    assert dw.error_bits() == 0
+    step = wl.steps[0]
+    ds = dw.steps[0]
+    kp, vp = oracle_e4m3_pools(wl, sc)
+    got = gpu_out(ds.out)
+    assert np.isfinite(got).all()
+    n = step.rows_upper
+    rng = np.random.default_rng(56)
+    rows = sorted(set([0, 1, 2, 3, n - 1] + rng.choice(n, size=4, replace=False).tolist()))
+    layers = [0, wl.layers - 1]
+    ref = oracle_e4m3_step_out(wl, step, kp, vp, sc, layers=layers, rows=rows)
+    assert np.abs(got[layers][:, rows] - ref).max() <= ATOL["bf16"]
+    again = torch.empty_like(ds.out[1])
+    dw.attend(ds, 1, out=again)
+    torch.cuda.synchronize()
+    assert torch.equal(again.view(torch.int16), ds.out[1].view(torch.int16))
